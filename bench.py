@@ -1,0 +1,510 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-attention hot path on GB300.
+
+One step = one pass of the decode hot path over one batch: append this step's
+new K/V rows into the paged cache (paged_kv_store) and run paged attention over
+every query (paged_attn_forward_split with the library's split heuristic, which
+launches the split-KV decode kernel and, when splits > 1, the LSE merge).  The
+schedule is built and uploaded once before timing (it is reused while the
+schedule is unchanged); the end-to-end leg re-uploads it every step.
+
+Main line: the Llama-3-8B-like GQA decode layer -- 64 sequences, one query each,
+Hq=32, Hkv=8, D=Dv=128, page_size=16, contexts U[512, 8192], bf16, shuffled
+pages.  Its KV working set (~1.1 GB) exceeds the 129 MB L2, so no flush is
+needed between steps.  Metric: KV-cache bytes the step must read (sum over
+queries of visible keys x Hkv x (D + Dv) x 2 B) per second, plus queries/s.
+
+Secondary measurements (same JSON line, key "workloads"): long-context split
+decode (contexts 32K..128K, Hq=64, split sweep), mixed chunked prefill +
+decode (TFLOP/s on causal-visible pairs), and MLA decode (TFLOP/s and KV GB/s).
+
+--impl reference times the fp64 CPU oracle on the host cores on bounded samples
+of the same workload (there is no other implementation to compare with).
+Multi-GPU: independent replicas (no exchange step exists), weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV GB/s (% HBM peak), queries/s; prefill/MLA TFLOP/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------- helpers --
+
+def visible_counts(case) -> np.ndarray:
+    if case.causal:
+        return case.query_pos.astype(np.int64) + 1
+    return case.seq_lens[case.query_seq].astype(np.int64)
+
+
+def kv_bytes(case) -> int:
+    """Algorithmic K/V bytes: each query's visible keys, each KV head read once."""
+    elt = torch.empty((), dtype=case.dtype).element_size()
+    n = int(visible_counts(case).sum())
+    if case.is_mla:
+        return n * (case.d + case.p) * elt
+    return n * case.hkv * (case.d + case.dv) * elt
+
+
+def attn_flops(case) -> int:
+    """Multiply-add flops over causal-visible (query, key) pairs."""
+    n = int(visible_counts(case).sum())
+    if case.is_mla:
+        return n * case.hq * (2 * (case.d + case.p) + 2 * case.d)
+    return n * case.hq * (2 * case.d + 2 * case.dv)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBps")
+            bf16 = d.get("bf16_tflops")
+            bf16s = d.get("bf16_tflops_sustained") or bf16
+            if hbm and bf16:
+                return {"hbm_gbs": float(hbm), "bf16_tflops": float(bf16), "bf16_tflops_sustained": float(bf16s),
+                        "source": "measured"}
+        except Exception:
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def profile_traffic(name: str, source_files):
+    """dram bytes per launch recorded in profiles/<name>.md, if the kernel source is unchanged."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", name + ".md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h:
+        return None
+    sha = hashlib.sha256()
+    for f in source_files:
+        sha.update(open(os.path.join(ROOT, f), "rb").read())
+    if sha.hexdigest()[:16] != h.group(1)[:16]:
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.tmp.flush()
+        rows = [r.split(",") for r in open(self.tmp.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# -------------------------------------------------------------- GPU steps --
+
+class DecodeStep:
+    """Resident inputs, plan, workspace and the two calls of one step."""
+
+    def __init__(self, case, device, splits=None):
+        import paged_kv_attention_20_gb300 as pka
+        self.pka = pka
+        self.case = case
+        self.dc = case.to(device)
+        self.plan = pka.paged_attn_plan(case.seq_lens, case.block_table, case.query_seq, case.query_pos,
+                                        case.page_size, case.num_pages, device=device)
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        self.splits = splits or pka.paged_attn_split_heuristic(self.plan, case.hq, case.hkv, sms)
+        self.ws = pka.make_workspace(self.plan, case.hq, case.dv, max(self.splits, 1), device)
+        self.out = torch.empty(case.num_queries, case.hq, case.dv, dtype=case.dtype, device=device)
+
+    def store(self):
+        d = self.dc
+        self.pka.paged_kv_store(self.plan, d.new_k, d.new_v, d.k_cache, d.v_cache)
+
+    def attend(self):
+        d = self.dc
+        if self.case.is_mla:
+            self.pka.paged_mla_forward(self.plan, d.q, d.qp, d.k_cache, d.v_cache, self.case.scale,
+                                       causal=self.case.causal, workspace=self.ws, splits=self.splits,
+                                       out=self.out)
+        else:
+            self.pka.paged_attn_forward_split(self.plan, d.q, d.k_cache, d.v_cache, self.case.scale,
+                                              self.splits, workspace=self.ws, causal=self.case.causal,
+                                              out=self.out)
+
+    def kernels_per_step(self) -> int:
+        return 2 + (1 if self.splits > 1 else 0) + (1 if (self.plan.n_tiles and not self.case.is_mla) else 0)
+
+
+def time_step(step: DecodeStep, steps: int, warmup: int, world: int, device, sampler=None):
+    for _ in range(warmup):
+        step.store()
+        step.attend()
+    torch.cuda.synchronize(device)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.start()
+    t0.record()
+    for i in range(steps):
+        evs[i][0].record()
+        step.store()
+        evs[i][1].record()
+        step.attend()
+        evs[i][2].record()
+    t1.record()
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop() if sampler else None
+    barrier(world)
+    total = t0.elapsed_time(t1)
+    store_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    return total, store_ms, attn_ms, clocks
+
+
+def soak_clocks(step: DecodeStep, device, seconds=1.0):
+    sampler = ClockSampler(device.index or 0).start()
+    time.sleep(0.2)
+    t_end = time.time() + seconds
+    while time.time() < t_end:
+        for _ in range(20):
+            step.store()
+            step.attend()
+        torch.cuda.synchronize(device)
+    c = sampler.stop()
+    c["window"] = "load soak right after the timed region"
+    return c
+
+
+def e2e_leg(case, device, steps: int, warmup: int):
+    """Same metric through the public API with host buffers: per step, upload the
+    plan and this step's inputs from pinned memory, append, attend, read the
+    result back (pinned) and wait for it."""
+    import paged_kv_attention_20_gb300 as pka
+    step = DecodeStep(case, device)
+    host = {k: getattr(case, k).pin_memory() for k in ("q", "new_k", "new_v")}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    words = step.plan.words
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + step.plan.device_bytes()
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        step.plan.upload_into(words)
+        step.dc.q.copy_(host["q"], non_blocking=True)
+        step.dc.new_k.copy_(host["new_k"], non_blocking=True)
+        step.dc.new_v.copy_(host["new_v"], non_blocking=True)
+        step.store()
+        step.attend()
+        out_host.copy_(step.out, non_blocking=True)
+        torch.cuda.current_stream(device).synchronize()
+
+    for _ in range(warmup):
+        one()
+    t = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t
+    del pka
+    return {"value": kv_bytes(case) * steps / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": dt / steps * 1e3}
+
+
+def secondary(device, warmup: int, steps: int, peaks, which):
+    """Long-context split decode, mixed prefill + decode, MLA decode (one entry each)."""
+    import workloads
+    res = {}
+    hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    if "long" in which:
+        res.update(_long_context(device, warmup, steps, hbm))
+    for name, maker in (("mixed_prefill_decode_bf16", workloads.mixed_prefill_decode_bf16),
+                        ("mla_decode_bf16", workloads.mla_decode_bf16)):
+        if name.split("_")[0] not in which:
+            continue
+        case = maker()
+        st = DecodeStep(case, device)
+        for _ in range(warmup):
+            st.store()
+            st.attend()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            st.attend()
+        e1.record()
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1) / steps
+        fl = attn_flops(case)
+        res[name] = {"queries": case.num_queries, "splits": st.splits, "ms": ms, "flops": fl,
+                     "tflops": fl / ms / 1e9, "frac_bf16_peak": fl / ms / 1e9 / tc,
+                     "kv_gbs": kv_bytes(case) / ms / 1e6, "frac_hbm": kv_bytes(case) / ms / 1e6 / hbm,
+                     "prefill_tiles": st.plan.n_tiles, "decode_items": st.plan.n_decode}
+        del st, case
+        torch.cuda.empty_cache()
+    return res
+
+
+def _long_context(device, warmup, steps, hbm):
+    import workloads
+    res = {}
+    c3 = workloads.long_context_decode_bf16()
+    sweep = {}
+    for s in (None, 1, 4, 8, 16, 32, 64):
+        st = DecodeStep(c3, device, splits=s)
+        for _ in range(warmup):
+            st.attend()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            st.attend()
+        e1.record()
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1) / steps
+        sweep["heuristic" if s is None else str(s)] = {"splits": st.splits, "ms": ms,
+                                                        "kv_gbs": kv_bytes(c3) / ms / 1e6}
+        del st
+    best = max(sweep.values(), key=lambda r: r["kv_gbs"])
+    h = sweep["heuristic"]
+    res["long_context_split_decode_bf16"] = {
+        "config": "4 seqs ctx {32K,64K,96K,128K}, Hq=64, Hkv=8, D=128, ps=16, bf16",
+        "kv_bytes": kv_bytes(c3), "heuristic_splits": h["splits"], "ms": h["ms"], "kv_gbs": h["kv_gbs"],
+        "frac_hbm": h["kv_gbs"] / hbm, "best_splits": best["splits"], "best_kv_gbs": best["kv_gbs"],
+        "sweep": sweep}
+    del c3
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def oracle_rows_rate(case, rows, nthreads=0):
+    """Run the oracle on flat (q*Hq+h) rows; return (seconds, algorithmic KV bytes covered)."""
+    import oracle
+    q_of = np.asarray(rows) // case.hq
+    vis = visible_counts(case)[q_of]
+    elt = torch.empty((), dtype=case.dtype).element_size()
+    per_row = case.hkv * (case.d + case.dv) * elt / case.hq       # each row's share of its query's bytes
+    t = time.perf_counter()
+    oracle.attention(case.q, case.k_cache, case.v_cache, case.seq_lens, case.block_table, case.query_seq,
+                     case.query_pos, case.scale, rows=rows, nthreads=nthreads)
+    return time.perf_counter() - t, float(vis.sum() * per_row)
+
+
+def cpu_baseline(case, budget_s=15.0):
+    import oracle
+    threads = oracle.threads()
+    nrows = case.num_queries * case.hq
+    probe = np.arange(min(nrows, max(threads, 32)))
+    t, b = oracle_rows_rate(case, probe)
+    rate = b / max(t, 1e-9)
+    want = int(min(nrows, max(len(probe), len(probe) * budget_s / max(t, 1e-6))))
+    rows = np.linspace(0, nrows - 1, want).astype(np.int64)
+    rows = np.unique(rows)
+    t, b = oracle_rows_rate(case, rows)
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} of {nrows} (query, head) rows of the GQA decode workload, evenly spaced; "
+                      f"{t:.1f} s on {threads} threads"}
+
+
+def reference_arm(args, rank, world):
+    """The oracle as the reference implementation: bounded samples per step, host cores."""
+    if world > 1 and rank != 0:
+        return
+    import oracle
+    import workloads
+    case = workloads.gqa_decode_bf16()
+    threads = oracle.threads()
+    nrows = case.num_queries * case.hq
+    probe = np.arange(min(nrows, max(threads, 32)))
+    t, _ = oracle_rows_rate(case, probe)
+    per_row = t / len(probe)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    k = int(max(threads, min(nrows, budget / max(per_row, 1e-9))))
+    k = min(k, nrows)
+    times, bytes_ = [], []
+    for i in range(args.warmup + args.steps):
+        rows = (np.arange(k) * 97 + i * k) % nrows
+        rows = np.unique(rows)
+        dt, b = oracle_rows_rate(case, rows)
+        if i >= args.warmup:
+            times.append(dt)
+            bytes_.append(b)
+    value = sum(bytes_) / sum(times) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sum(times) / len(times) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "gqa_decode_bf16: 64 seqs x 1 query, Hq=32, Hkv=8, D=Dv=128, ps=16, "
+                                   "ctx U[512,8192], bf16 inputs", "l2": "inputs larger than L2"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{k} (query, head) rows per step of the same workload"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- main --
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--secondary", default="long,mixed,mla",
+                    help="comma list of secondary workloads: long, mixed, mla ('' for none)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=None, help="override the split heuristic")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_info()
+
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    import paged_kv_attention_20_gb300 as pka
+    import workloads
+    pka.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    peaks = measured_peaks()
+    case = workloads.gqa_decode_bf16()
+    step = DecodeStep(case, device, splits=args.splits)
+    sampler = ClockSampler(device.index or 0) if rank == 0 else None
+    total_ms, store_ms, attn_ms, clocks = time_step(step, args.steps, args.warmup, world, device, sampler)
+    total_ms = max_over_ranks(total_ms, world, device)
+    if rank == 0 and clocks is not None and clocks.get("samples", 0) < 3:
+        clocks = soak_clocks(step, device)
+
+    kvb = kv_bytes(case)
+    ms_per_step = total_ms / args.steps
+    value = world * kvb * args.steps / (total_ms / 1e3) / 1e9
+    attn_mean = statistics.mean(attn_ms)
+    achieved = kvb / (attn_mean / 1e3) / 1e9
+    traffic = profile_traffic("decode_fast_gqa_decode_bf16",
+                              ["paged_kv_attention_20_gb300/csrc/decode.cu"])
+
+    if rank != 0:
+        barrier(world)
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "gqa_decode_bf16: 64 seqs x 1 decode query, Hq=32, Hkv=8, D=Dv=128, "
+                               "page_size=16, ctx U[512,8192] (seed 2), shuffled pages, bf16, fp32 accumulate",
+                   "step": "paged_kv_store + paged_attn_forward_split (heuristic splits) on resident inputs",
+                   "splits": step.splits, "kv_bytes_per_step": kvb, "queries_per_step": case.num_queries,
+                   "l2": "inputs larger than L2 (KV working set ~1.1 GB > 129 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "queries_per_s": world * case.num_queries * args.steps / (total_ms / 1e3),
+        "frac_hbm_peak": value / world / peaks["hbm_gbs"],
+        "kernel_ms": {"store": statistics.mean(store_ms), "attention": attn_mean},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "decode_fast_kernel<bf16,128,4> (+ merge when splits > 1)",
+                     "peak_source": f"{peaks['source']} HBM copy bandwidth"},
+        "clocks": clocks,
+        "gpu_launches": args.steps * step.kernels_per_step(),
+    }
+    del step
+    torch.cuda.empty_cache()
+    line["e2e"] = e2e_leg(case, device, steps=max(10, min(args.steps, 200)), warmup=args.warmup)
+    which = [w for w in args.secondary.split(",") if w]
+    if which:
+        line["workloads"] = secondary(device, args.warmup, 20, peaks, which)
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case.to("cpu"))
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,67 @@
+// Internal declarations shared by the host library and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "paged_attn.h"
+
+namespace pa {
+
+// Work-list constants of the plan.
+constexpr int kPrefillTileM = 128;   // queries per tensor-core prefill tile
+constexpr int kPrefillMinRun = 16;   // shorter runs of consecutive positions stay decode items
+
+// Device view of an uploaded plan.  Every array lives in the caller's
+// metadata buffer; offsets are fixed by the host plan (see plan.cpp).
+struct PlanView {
+    const int4 *qmeta;       // [queries] {seq, pos, physical slot, 0}
+    const int32_t *seq_lens; // [sequences]
+    const int32_t *table;    // [sequences * width]
+    const int32_t *decode;   // [n_decode] query indices handled by the decode kernel
+    const int4 *tiles;       // [n_tiles] {seq, first query, query count, first position}
+    int32_t queries;
+    int32_t sequences;
+    int32_t width;
+    int32_t page_size;
+    int32_t pages;
+    int32_t n_decode;
+    int32_t n_tiles;
+};
+
+// Arguments common to the attention kernels.
+struct AttnArgs {
+    PlanView plan;
+    const void *q;        // [Q, Hq, D]
+    const void *k;        // [pages, ps, Hkv, D]   (MLA: latent [pages, ps, 1, R])
+    const void *v;        // [pages, ps, Hkv, Dv]  (MLA: same latent pointer)
+    const void *qp;       // MLA position query [Q, Hq, P] or null
+    const void *kp;       // MLA position cache [pages, ps, 1, P] or null
+    void *out;            // [Q, Hq, Dv] in the operand dtype
+    float *ws_o;          // split partials [S, Q, Hq, Dv] fp32 (null when unsplit)
+    float *ws_lse;        // split lse      [S, Q, Hq]     fp32
+    int32_t hq, hkv, d, dv, p;
+    float scale;
+    int32_t causal;
+    int32_t splits;
+    pa_dtype dtype;
+};
+
+// Launchers (return cudaGetLastError() of the launch).
+// use_decode_list: iterate over plan.decode (else over every query).
+cudaError_t launch_kv_store(const PlanView &plan, const void *new_k, const void *new_v, void *k_cache,
+                            void *v_cache, int heads, int d, int dv, int elem_bytes, cudaStream_t st);
+cudaError_t launch_decode(const AttnArgs &a, bool use_decode_list, cudaStream_t st);
+cudaError_t launch_merge(const AttnArgs &a, bool use_decode_list, cudaStream_t st);
+// Tensor-core prefill over plan.tiles; returns cudaErrorNotSupported when the
+// shape/dtype is outside what the kernel covers (caller then uses decode for all).
+bool prefill_supported(const AttnArgs &a);
+cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st);
+bool mla_supported(const AttnArgs &a);
+cudaError_t launch_mla(const AttnArgs &a, bool use_decode_list, cudaStream_t st);
+
+// Device status word (bounded waits record their timeouts here).
+cudaError_t read_device_status(int32_t *code, bool clear);
+
+}  // namespace pa

@@ -1,0 +1,395 @@
+// Host side of the paged-attention library: schedule building and
+// validation, argument checks, dispatch to the kernels, and the C ABI.
+//
+// Follows ruDNN 0.1.7, src/paged_attention/mod.rs: `HostPlan` /
+// `DevicePlan::upload` (one small upload of u32 metadata, reusable while the
+// schedule is unchanged), `check_tensor` / `bounded` and
+// `execute_attention_into` (every check happens before any launch; zero
+// queries is a successful no-op), `append_with_report` (`validate_writes`,
+// then an elementwise append), and the split path (`attention_into_split`:
+// attention over (item, head, split) then a merge when splits > 1).
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "pa_internal.h"
+
+struct pa_plan {
+    int32_t queries = 0, sequences = 0, width = 0, page_size = 0, pages = 0;
+    int32_t n_decode = 0, n_tiles = 0, n_tile_queries = 0;
+    int64_t max_seq_len = 0;          // longest sequence any decode item reads
+    std::vector<int32_t> words;       // host copy of the device metadata
+    size_t off_qmeta = 0, off_seqlen = 0, off_table = 0, off_decode = 0, off_tiles = 0;
+    const int32_t *dev = nullptr;     // caller's device copy (after upload)
+};
+
+namespace {
+
+thread_local std::string g_error;
+
+pa_status fail(pa_status st, const char *msg) {
+    g_error = msg;
+    return st;
+}
+
+pa_status fail_cuda(cudaError_t e, const char *what) {
+    g_error = std::string(what) + ": " + cudaGetErrorString(e);
+    return PA_ERR_CUDA;
+}
+
+size_t align_words(size_t n, size_t a) { return (n + a - 1) / a * a; }
+
+bool valid_dtype(pa_dtype d) { return d == PA_F32 || d == PA_F16 || d == PA_BF16; }
+
+int elem_bytes(pa_dtype d) { return d == PA_F32 ? 4 : 2; }
+
+pa::PlanView view_of(const pa_plan *p) {
+    pa::PlanView v{};
+    v.qmeta = reinterpret_cast<const int4 *>(p->dev + p->off_qmeta);
+    v.seq_lens = p->dev + p->off_seqlen;
+    v.table = p->dev + p->off_table;
+    v.decode = p->dev + p->off_decode;
+    v.tiles = reinterpret_cast<const int4 *>(p->dev + p->off_tiles);
+    v.queries = p->queries;
+    v.sequences = p->sequences;
+    v.width = p->width;
+    v.page_size = p->page_size;
+    v.pages = p->pages;
+    v.n_decode = p->n_decode;
+    v.n_tiles = p->n_tiles;
+    return v;
+}
+
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_last_error(void) { return g_error.c_str(); }
+
+const char *pa_status_string(pa_status s) {
+    switch (s) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_ARG: return "PA_ERR_ARG";
+        case PA_ERR_SHAPE: return "PA_ERR_SHAPE";
+        case PA_ERR_DTYPE: return "PA_ERR_DTYPE";
+        case PA_ERR_RANGE: return "PA_ERR_RANGE";
+        case PA_ERR_WRITE_CONFLICT: return "PA_ERR_WRITE_CONFLICT";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_SPLITS: return "PA_ERR_SPLITS";
+        case PA_ERR_LIMIT: return "PA_ERR_LIMIT";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_STATE: return "PA_ERR_STATE";
+    }
+    return "PA_UNKNOWN";
+}
+
+int32_t pa_abi_version(void) { return PA_ABI_VERSION; }
+
+pa_status paged_attn_plan(const int32_t *seq_lens, int32_t num_seqs, const int32_t *block_table,
+                          int32_t width, const int32_t *query_seq, const int32_t *query_pos,
+                          int32_t num_queries, int32_t page_size, int32_t num_pages,
+                          pa_plan **out_plan) {
+    if (!out_plan) return fail(PA_ERR_ARG, "paged_attn_plan: out_plan is null");
+    *out_plan = nullptr;
+    if (num_seqs < 0 || width < 0 || num_queries < 0 || num_pages < 0)
+        return fail(PA_ERR_ARG, "paged_attn_plan: negative count");
+    if (page_size < 1) return fail(PA_ERR_ARG, "paged_attn_plan: page_size must be >= 1");
+    if ((int64_t)num_pages * page_size > INT32_MAX)
+        return fail(PA_ERR_RANGE, "paged_attn_plan: pages * page_size exceeds 32-bit slot indexing");
+    if ((int64_t)num_seqs * width > INT32_MAX / 2)
+        return fail(PA_ERR_RANGE, "paged_attn_plan: block table exceeds 32-bit indexing");
+    if (num_seqs > 0 && !seq_lens) return fail(PA_ERR_ARG, "paged_attn_plan: seq_lens is null");
+    if (num_seqs > 0 && width > 0 && !block_table)
+        return fail(PA_ERR_ARG, "paged_attn_plan: block_table is null");
+    if (num_queries > 0 && (!query_seq || !query_pos))
+        return fail(PA_ERR_ARG, "paged_attn_plan: query arrays are null");
+
+    // Sequences: length within the table, used table entries within the pool.
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int64_t n = seq_lens[s];
+        if (n < 0) return fail(PA_ERR_RANGE, "paged_attn_plan: negative sequence length");
+        if (n > (int64_t)width * page_size)
+            return fail(PA_ERR_RANGE, "paged_attn_plan: sequence longer than its block-table row");
+        int64_t used = (n + page_size - 1) / page_size;
+        for (int64_t g = 0; g < used; ++g) {
+            int32_t pg = block_table[(int64_t)s * width + g];
+            if (pg < 0 || pg >= num_pages)
+                return fail(PA_ERR_RANGE, "paged_attn_plan: block-table entry outside the page pool");
+        }
+    }
+    // Queries: valid sequence, 0 <= pos < seq_len; distinct write slots.
+    std::vector<int64_t> slots((size_t)num_queries);
+    for (int32_t i = 0; i < num_queries; ++i) {
+        int32_t s = query_seq[i], pos = query_pos[i];
+        if (s < 0 || s >= num_seqs) return fail(PA_ERR_RANGE, "paged_attn_plan: query sequence out of range");
+        if (pos < 0 || pos >= seq_lens[s])
+            return fail(PA_ERR_RANGE, "paged_attn_plan: query position outside its sequence");
+        int64_t pg = block_table[(int64_t)s * width + pos / page_size];
+        slots[(size_t)i] = pg * page_size + pos % page_size;
+    }
+    {
+        std::vector<int64_t> sorted = slots;
+        std::sort(sorted.begin(), sorted.end());
+        if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+            return fail(PA_ERR_WRITE_CONFLICT, "paged_attn_plan: two queries write the same cache slot");
+    }
+
+    pa_plan *p = new pa_plan();
+    p->queries = num_queries;
+    p->sequences = num_seqs;
+    p->width = width;
+    p->page_size = page_size;
+    p->pages = num_pages;
+
+    // Work lists: runs of consecutive positions of one sequence -> prefill
+    // tiles of up to kPrefillTileM queries; all other queries -> decode items.
+    std::vector<int32_t> decode;
+    std::vector<int32_t> tiles;  // 4 words per tile
+    int32_t i = 0;
+    while (i < num_queries) {
+        int32_t j = i + 1;
+        while (j < num_queries && query_seq[j] == query_seq[i] && query_pos[j] == query_pos[j - 1] + 1) ++j;
+        int32_t run = j - i;
+        if (run >= pa::kPrefillMinRun) {
+            for (int32_t b = i; b < j; b += pa::kPrefillTileM) {
+                int32_t cnt = std::min(pa::kPrefillTileM, j - b);
+                tiles.insert(tiles.end(), {query_seq[i], b, cnt, query_pos[b]});
+                p->n_tile_queries += cnt;
+            }
+        } else {
+            for (int32_t b = i; b < j; ++b) {
+                decode.push_back(b);
+                p->max_seq_len = std::max<int64_t>(p->max_seq_len, seq_lens[query_seq[b]]);
+            }
+        }
+        i = j;
+    }
+    p->n_decode = (int32_t)decode.size();
+    p->n_tiles = (int32_t)(tiles.size() / 4);
+
+    // Word layout (int32 words; 16-byte aligned sections):
+    //   [0..15]  header: magic, queries, sequences, width, page_size, pages,
+    //            n_decode, n_tiles, and the five section offsets
+    //   qmeta    queries x {seq, pos, slot, 0}
+    //   seqlen   sequences
+    //   table    sequences x width
+    //   decode   n_decode query indices
+    //   tiles    n_tiles x {seq, first query, count, first position}
+    size_t off = 16;
+    p->off_qmeta = off;   off = align_words(off + 4 * (size_t)num_queries, 4);
+    p->off_seqlen = off;  off = align_words(off + (size_t)num_seqs, 4);
+    p->off_table = off;   off = align_words(off + (size_t)num_seqs * width, 4);
+    p->off_decode = off;  off = align_words(off + decode.size(), 4);
+    p->off_tiles = off;   off = align_words(off + tiles.size(), 4);
+    p->words.assign(off, 0);
+    int32_t *w = p->words.data();
+    w[0] = 0x50414731;  // "PAG1"
+    w[1] = num_queries; w[2] = num_seqs; w[3] = width; w[4] = page_size; w[5] = num_pages;
+    w[6] = p->n_decode; w[7] = p->n_tiles;
+    w[8] = (int32_t)p->off_qmeta; w[9] = (int32_t)p->off_seqlen; w[10] = (int32_t)p->off_table;
+    w[11] = (int32_t)p->off_decode; w[12] = (int32_t)p->off_tiles; w[13] = (int32_t)off;
+    for (int32_t q = 0; q < num_queries; ++q) {
+        int32_t *m = w + p->off_qmeta + 4 * (size_t)q;
+        m[0] = query_seq[q];
+        m[1] = query_pos[q];
+        m[2] = (int32_t)slots[(size_t)q];
+        m[3] = 0;
+    }
+    if (num_seqs) std::memcpy(w + p->off_seqlen, seq_lens, sizeof(int32_t) * (size_t)num_seqs);
+    for (int64_t e = 0; e < (int64_t)num_seqs * width; ++e)
+        w[p->off_table + e] = block_table[e] < 0 ? 0 : block_table[e];  // unused entries never read
+    if (!decode.empty()) std::memcpy(w + p->off_decode, decode.data(), sizeof(int32_t) * decode.size());
+    if (!tiles.empty()) std::memcpy(w + p->off_tiles, tiles.data(), sizeof(int32_t) * tiles.size());
+    *out_plan = p;
+    return PA_OK;
+}
+
+size_t pa_plan_device_bytes(const pa_plan *plan) { return plan ? plan->words.size() * sizeof(int32_t) : 0; }
+
+pa_status pa_plan_upload(pa_plan *plan, void *device_words, size_t bytes, pa_stream_t stream) {
+    if (!plan || !device_words) return fail(PA_ERR_ARG, "pa_plan_upload: null argument");
+    if (!aligned16(device_words)) return fail(PA_ERR_ARG, "pa_plan_upload: device buffer not 16-byte aligned");
+    size_t need = pa_plan_device_bytes(plan);
+    if (bytes < need) return fail(PA_ERR_ARG, "pa_plan_upload: device buffer too small");
+    cudaError_t e = cudaMemcpyAsync(device_words, plan->words.data(), need, cudaMemcpyHostToDevice,
+                                    (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(e, "pa_plan_upload");
+    plan->dev = static_cast<const int32_t *>(device_words);
+    return PA_OK;
+}
+
+void pa_plan_destroy(pa_plan *plan) { delete plan; }
+
+pa_status pa_plan_describe(const pa_plan *plan, int64_t out[8]) {
+    if (!plan || !out) return fail(PA_ERR_ARG, "pa_plan_describe: null argument");
+    out[0] = plan->queries; out[1] = plan->sequences; out[2] = plan->width; out[3] = plan->page_size;
+    out[4] = plan->pages; out[5] = plan->n_decode; out[6] = plan->n_tiles; out[7] = plan->n_tile_queries;
+    return PA_OK;
+}
+
+size_t pa_workspace_bytes(int32_t queries, int32_t heads, int32_t value_dim, int32_t splits) {
+    if (queries < 0 || heads < 1 || value_dim < 1 || splits < 1) return 0;
+    size_t rows = (size_t)splits * (size_t)queries * (size_t)heads;
+    size_t o = (rows * (size_t)value_dim * sizeof(float) + 255) / 256 * 256;
+    size_t l = (rows * sizeof(float) + 255) / 256 * 256;
+    return o + l;
+}
+
+int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t num_kv_heads,
+                                   int32_t num_sms) {
+    if (!plan || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads || num_sms < 1) return 1;
+    int64_t items = plan->n_decode;
+    if (items == 0) return 1;
+    int64_t group = num_heads / num_kv_heads;
+    int64_t blocks = items * num_kv_heads * ((group + 7) / 8);
+    int64_t target = 4 * (int64_t)num_sms;
+    int64_t s = (target + blocks - 1) / blocks;
+    int64_t cap = std::max<int64_t>(1, plan->max_seq_len / (4 * (int64_t)plan->page_size));
+    s = std::min<int64_t>(s, cap);
+    s = std::max<int64_t>(1, std::min<int64_t>(s, PA_MAX_SPLITS));
+    return (int32_t)s;
+}
+
+pa_status paged_kv_store(const pa_plan *plan, const void *new_k, const void *new_v, void *k_cache,
+                         void *v_cache, int32_t num_heads, int32_t head_dim, int32_t value_dim,
+                         pa_dtype dtype, pa_stream_t stream) {
+    if (!plan) return fail(PA_ERR_ARG, "paged_kv_store: plan is null");
+    if (!valid_dtype(dtype)) return fail(PA_ERR_DTYPE, "paged_kv_store: dtype must be F32, F16 or BF16");
+    if (num_heads < 1 || head_dim < 1 || value_dim < 1)
+        return fail(PA_ERR_SHAPE, "paged_kv_store: heads, head_dim and value_dim must be >= 1");
+    if ((int64_t)plan->pages * plan->page_size * num_heads * std::max(head_dim, value_dim) > (int64_t)1 << 40)
+        return fail(PA_ERR_RANGE, "paged_kv_store: cache too large");
+    if (plan->queries == 0) return PA_OK;  // no-op append
+    if (!plan->dev) return fail(PA_ERR_STATE, "paged_kv_store: plan not uploaded");
+    if (!new_k || !new_v || !k_cache || !v_cache) return fail(PA_ERR_ARG, "paged_kv_store: null tensor");
+    cudaError_t e = pa::launch_kv_store(view_of(plan), new_k, new_v, k_cache, v_cache, num_heads, head_dim,
+                                        value_dim, elem_bytes(dtype), (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(e, "paged_kv_store launch");
+    return PA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared body of the attention entry points.
+pa_status attention(const pa_plan *plan, const void *q, const void *k, const void *v, const void *qp,
+                    const void *kp, void *out, int32_t hq, int32_t hkv, int32_t d, int32_t dv, int32_t p,
+                    float scale, int32_t causal, pa_dtype dtype, void *ws, size_t ws_bytes, int32_t splits,
+                    bool split_call, bool mla, cudaStream_t st, const char *name) {
+    char msg[256];
+    auto bad = [&](pa_status s, const char *what) {
+        std::snprintf(msg, sizeof msg, "%s: %s", name, what);
+        return fail(s, msg);
+    };
+    if (!plan) return bad(PA_ERR_ARG, "plan is null");
+    if (!valid_dtype(dtype)) return bad(PA_ERR_DTYPE, "dtype must be F32, F16 or BF16");
+    if (hq < 1 || hkv < 1 || hq % hkv != 0) return bad(PA_ERR_SHAPE, "num_heads must be a positive multiple of num_kv_heads");
+    if (d < 1 || dv < 1) return bad(PA_ERR_SHAPE, "head dims must be >= 1");
+    if (d > PA_MAX_HEAD_DIM || dv > PA_MAX_HEAD_DIM) return bad(PA_ERR_LIMIT, "head dim above 1024");
+    if (!std::isfinite(scale) || !(scale > 0.f)) return bad(PA_ERR_SHAPE, "scale must be finite and > 0");
+    if (causal != 0 && causal != 1) return bad(PA_ERR_ARG, "causal must be 0 or 1");
+    if (mla) {
+        if (p < 1 || p > PA_MAX_POS_DIM) return bad(PA_ERR_LIMIT, "MLA position dim must be in 1..256");
+    }
+    if (hq > 65535) return bad(PA_ERR_LIMIT, "num_heads above the launch grid limit");
+    if ((int64_t)plan->queries * hq * std::max(d, dv) > ((int64_t)1 << 40))
+        return bad(PA_ERR_RANGE, "tensor too large");
+    if (split_call) {
+        if (splits < 1 || splits > PA_MAX_SPLITS) return bad(PA_ERR_SPLITS, "splits must be in 1..64");
+        if (splits > 1 || ws) {
+            size_t need = pa_workspace_bytes(plan->queries, hq, dv, splits);
+            if (need > PA_WORKSPACE_LIMIT_BYTES) return bad(PA_ERR_WORKSPACE, "workspace above the 1 GiB limit");
+            if (splits > 1 && !ws) return bad(PA_ERR_WORKSPACE, "workspace is null");
+            if (ws && ws_bytes < need) return bad(PA_ERR_WORKSPACE, "workspace too small");
+            if (ws && !aligned16(ws)) return bad(PA_ERR_WORKSPACE, "workspace not 16-byte aligned");
+        }
+    } else {
+        splits = 1;
+    }
+    if (plan->queries == 0) return PA_OK;  // nothing to launch
+    if (!plan->dev) return bad(PA_ERR_STATE, "plan not uploaded");
+    if (!q || !k || !v || !out || (mla && (!qp || !kp))) return bad(PA_ERR_ARG, "null tensor");
+
+    pa::AttnArgs a{};
+    a.plan = view_of(plan);
+    a.q = q; a.k = k; a.v = v; a.qp = qp; a.kp = kp; a.out = out;
+    a.hq = hq; a.hkv = hkv; a.d = d; a.dv = dv; a.p = mla ? p : 0;
+    a.scale = scale; a.causal = causal; a.splits = splits; a.dtype = dtype;
+    if (splits > 1) {
+        size_t rows = (size_t)splits * plan->queries * hq;
+        a.ws_o = static_cast<float *>(ws);
+        a.ws_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + (rows * dv * sizeof(float) + 255) / 256 * 256);
+    }
+
+    cudaError_t e = cudaSuccess;
+    if (mla) {
+        bool fast = pa::mla_supported(a);
+        e = fast ? pa::launch_mla(a, false, st) : pa::launch_decode(a, false, st);
+        if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, false, st);
+    } else {
+        bool tiles = plan->n_tiles > 0 && pa::prefill_supported(a);
+        if (tiles) {
+            e = pa::launch_prefill(a, st);
+            if (e == cudaSuccess && plan->n_decode > 0) {
+                e = pa::launch_decode(a, true, st);
+                if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, true, st);
+            }
+        } else {
+            e = pa::launch_decode(a, false, st);
+            if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, false, st);
+        }
+    }
+    if (e != cudaSuccess) return fail_cuda(e, name);
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status paged_attn_forward(const pa_plan *plan, const void *q, const void *k_cache, const void *v_cache,
+                             void *out, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t value_dim, float scale, int32_t causal, pa_dtype dtype,
+                             pa_stream_t stream) {
+    return attention(plan, q, k_cache, v_cache, nullptr, nullptr, out, num_heads, num_kv_heads, head_dim,
+                     value_dim, 0, scale, causal, dtype, nullptr, 0, 1, false, false, (cudaStream_t)stream,
+                     "paged_attn_forward");
+}
+
+pa_status paged_attn_forward_split(const pa_plan *plan, const void *q, const void *k_cache,
+                                   const void *v_cache, void *out, int32_t num_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t value_dim, float scale, int32_t causal,
+                                   pa_dtype dtype, void *workspace, size_t workspace_bytes, int32_t splits,
+                                   pa_stream_t stream) {
+    if (!workspace) return fail(PA_ERR_WORKSPACE, "paged_attn_forward_split: workspace is null");
+    return attention(plan, q, k_cache, v_cache, nullptr, nullptr, out, num_heads, num_kv_heads, head_dim,
+                     value_dim, 0, scale, causal, dtype, workspace, workspace_bytes, splits, true, false,
+                     (cudaStream_t)stream, "paged_attn_forward_split");
+}
+
+pa_status paged_mla_forward(const pa_plan *plan, const void *q, const void *qp, const void *latent_cache,
+                            const void *pos_cache, void *out, int32_t num_heads, int32_t latent_dim,
+                            int32_t pos_dim, float scale, int32_t causal, pa_dtype dtype, void *workspace,
+                            size_t workspace_bytes, int32_t splits, pa_stream_t stream) {
+    if (!workspace && splits != 1)
+        return fail(PA_ERR_SPLITS, "paged_mla_forward: splits must be 1 without a workspace");
+    return attention(plan, q, latent_cache, latent_cache, qp, pos_cache, out, num_heads, 1, latent_dim,
+                     latent_dim, pos_dim, scale, causal, dtype, workspace, workspace_bytes, splits, true, true,
+                     (cudaStream_t)stream, "paged_mla_forward");
+}
+
+pa_status pa_device_status(int32_t *code, int32_t clear) {
+    if (!code) return fail(PA_ERR_ARG, "pa_device_status: code is null");
+    cudaError_t e = pa::read_device_status(code, clear != 0);
+    if (e != cudaSuccess) return fail_cuda(e, "pa_device_status");
+    return PA_OK;
+}
+
+}  // extern "C"

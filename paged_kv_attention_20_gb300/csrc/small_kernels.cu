@@ -1,0 +1,138 @@
+// Cache append, split merge and the device status word.
+//
+// Append: ruDNN 0.1.7, src/paged_attention/mod.rs, `append_with_report` --
+// new rows [queries, heads, d|dv] land in the caches at the plan's positions,
+// an elementwise kernel over queries * heads * max(d, dv).  Here each thread
+// moves one 16-byte chunk (or one element when rows are not 16-byte multiples
+// or not aligned); the destination slot comes precomputed in the plan.
+//
+// Merge: same page, `execute_attention_into` (merge launch when splits > 1)
+// and `attention_into_split` (FP32 statistics): out = sum_s w_s o_s / sum_s w_s
+// with w_s = exp(lse_s - max_s lse_s); empty splits (lse = -inf) weigh 0.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+__device__ int32_t g_device_status = 0;
+
+template <typename U>
+__global__ void kv_store_kernel(PlanView plan, const U *__restrict__ new_k, const U *__restrict__ new_v,
+                                U *__restrict__ kc, U *__restrict__ vc, int heads, int uk, int uv,
+                                int64_t total) {
+    // One work unit = one U-sized piece of one row; K pieces then V pieces per (query, head).
+    const int per_row = uk + uv;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        int64_t row = idx / per_row;          // (query, head)
+        int u = (int)(idx - row * per_row);
+        int64_t qi = row / heads;
+        int h = (int)(row - qi * heads);
+        int64_t slot = plan.qmeta[qi].z;
+        if (u < uk) {
+            kc[(slot * heads + h) * uk + u] = new_k[row * uk + u];
+        } else {
+            u -= uk;
+            vc[(slot * heads + h) * uv + u] = new_v[row * uv + u];
+        }
+    }
+}
+
+cudaError_t launch_kv_store(const PlanView &plan, const void *new_k, const void *new_v, void *k_cache,
+                            void *v_cache, int heads, int d, int dv, int elem_bytes, cudaStream_t st) {
+    const int64_t kb = (int64_t)d * elem_bytes, vb = (int64_t)dv * elem_bytes;
+    auto al = [](const void *p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
+    int unit = elem_bytes;
+    if (kb % 16 == 0 && vb % 16 == 0 && al(new_k, 16) && al(new_v, 16) && al(k_cache, 16) && al(v_cache, 16))
+        unit = 16;
+    const int uk = (int)(kb / unit), uv = (int)(vb / unit);
+    const int64_t total = (int64_t)plan.queries * heads * (uk + uv);
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 152 * 32) blocks = 152 * 32;
+    if (blocks < 1) blocks = 1;
+    if (unit == 16)
+        kv_store_kernel<uint4><<<(unsigned)blocks, threads, 0, st>>>(
+            plan, (const uint4 *)new_k, (const uint4 *)new_v, (uint4 *)k_cache, (uint4 *)v_cache, heads, uk, uv, total);
+    else if (unit == 4)
+        kv_store_kernel<uint32_t><<<(unsigned)blocks, threads, 0, st>>>(
+            plan, (const uint32_t *)new_k, (const uint32_t *)new_v, (uint32_t *)k_cache, (uint32_t *)v_cache, heads,
+            uk, uv, total);
+    else
+        kv_store_kernel<uint16_t><<<(unsigned)blocks, threads, 0, st>>>(
+            plan, (const uint16_t *)new_k, (const uint16_t *)new_v, (uint16_t *)k_cache, (uint16_t *)v_cache, heads,
+            uk, uv, total);
+    return cudaGetLastError();
+}
+
+template <typename T> __device__ __forceinline__ T from_float(float x);
+template <> __device__ __forceinline__ float from_float<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// grid (items, Hq), 128 threads over the value dim.
+template <typename T>
+__global__ void __launch_bounds__(128) merge_kernel(AttnArgs a, int use_list) {
+    const int item = blockIdx.x, h = blockIdx.y;
+    const int qi = use_list ? a.plan.decode[item] : item;
+    const int S = a.splits;
+    __shared__ float w[PA_MAX_SPLITS];
+    __shared__ float wsum;
+    const int64_t rows = (int64_t)a.plan.queries * a.hq;
+    const int64_t row = (int64_t)qi * a.hq + h;
+    if (threadIdx.x < 32) {
+        // max and weights over the splits, one warp
+        float m = -INFINITY;
+        for (int s = threadIdx.x; s < S; s += 32) m = fmaxf(m, a.ws_lse[s * rows + row]);
+        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float tot = 0.f;
+        for (int s = threadIdx.x; s < S; s += 32) {
+            float l = a.ws_lse[s * rows + row];
+            float ws = (l == -INFINITY) ? 0.f : __expf(l - m);
+            w[s] = ws;
+            tot += ws;
+        }
+        for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (threadIdx.x == 0) wsum = tot;
+    }
+    __syncthreads();
+    const float inv = 1.f / wsum;
+    T *out = static_cast<T *>(a.out) + row * a.dv;
+    for (int c = threadIdx.x; c < a.dv; c += blockDim.x) {
+        float acc = 0.f;
+        for (int s = 0; s < S; ++s) {
+            float ws = w[s];
+            if (ws != 0.f) acc += ws * a.ws_o[(s * rows + row) * a.dv + c];
+        }
+        out[c] = from_float<T>(acc * inv);
+    }
+}
+
+cudaError_t launch_merge(const AttnArgs &a, bool use_list, cudaStream_t st) {
+    const int items = use_list ? a.plan.n_decode : a.plan.queries;
+    if (items == 0) return cudaSuccess;
+    dim3 grid(items, a.hq);
+    switch (a.dtype) {
+        case PA_F32: merge_kernel<float><<<grid, 128, 0, st>>>(a, use_list); break;
+        case PA_F16: merge_kernel<__half><<<grid, 128, 0, st>>>(a, use_list); break;
+        default: merge_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(a, use_list); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t read_device_status(int32_t *code, bool clear) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(code, g_device_status, sizeof(int32_t));
+    if (e != cudaSuccess) return e;
+    if (clear) {
+        int32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int32_t));
+    }
+    return e;
+}
+
+}  // namespace pa

@@ -1,0 +1,160 @@
+"""Host-only checks of the C ABI (no GPU calls).
+
+* libpagedattn.so loads and exports every function include/paged_attn.h declares;
+* schedule validation (ruDNN 0.1.7, src/paged_attention/mod.rs, `HostPlan` use,
+  `validate_writes`, `bounded`) rejects bad input with the documented status;
+* argument checks of the attention entry points (`execute_attention_into`)
+  fire before anything touches the device;
+* the work lists, workspace sizing and split heuristic behave as documented.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_attention_20_gb300 as pka
+from paged_kv_attention_20_gb300._binding import PagedAttentionError
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "paged_attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if not n.startswith("defined")))
+
+
+def test_header_functions_are_exported(built_lib):
+    names = declared_functions()
+    assert "paged_attn_forward" in names and "paged_kv_store" in names and len(names) >= 15
+    for n in names:
+        assert hasattr(built_lib, n), f"{n} declared in paged_attn.h but not exported"
+    assert set(pka.EXPORTED) <= set(names)
+    assert built_lib.pa_abi_version() == 1
+
+
+def _status_of(fn, *a, **k):
+    with pytest.raises(PagedAttentionError) as ei:
+        fn(*a, **k)
+    return ei.value.status
+
+
+def plan(*a, **k):
+    return pka.paged_attn_plan(*a, upload=False, **k)
+
+
+def test_plan_validation_statuses(built_lib):
+    ok = plan([5, 20], [[0, 1], [2, 3]], [0, 1], [4, 19], 16, 4)
+    assert ok.queries == 2 and ok.n_decode == 2 and ok.n_tiles == 0
+    # page id outside the pool
+    assert _status_of(plan, [5, 20], [[0, 1], [2, 9]], [0, 1], [4, 19], 16, 4) == 4
+    # position beyond the sequence
+    assert _status_of(plan, [5, 20], [[0, 1], [2, 3]], [0, 1], [5, 19], 16, 4) == 4
+    # negative position
+    assert _status_of(plan, [5, 20], [[0, 1], [2, 3]], [0, 1], [-1, 19], 16, 4) == 4
+    # sequence longer than its table row
+    assert _status_of(plan, [5, 40], [[0, 1], [2, 3]], [0, 1], [4, 19], 16, 4) == 4
+    # query names a missing sequence
+    assert _status_of(plan, [5, 20], [[0, 1], [2, 3]], [0, 2], [4, 19], 16, 4) == 4
+    # two queries of one plan write the same slot (also across sequences sharing a page)
+    assert _status_of(plan, [5, 20], [[0, 1], [2, 3]], [1, 1], [19, 19], 16, 4) == 5
+    assert _status_of(plan, [5, 5], [[0, 1], [0, 3]], [0, 1], [4, 4], 16, 4) == 5
+    # page_size must be positive
+    assert _status_of(plan, [5], [[0]], [0], [4], 0, 4) == 1
+    # slot indexing beyond 32 bits
+    assert _status_of(plan, [5], [[0]], [0], [4], 1 << 16, 1 << 16) == 4
+
+
+def test_shared_pages_for_reads_are_allowed(built_lib):
+    # two sequences share physical page 0 as a common prefix; they write different pages
+    p = plan([20, 20], [[0, 1], [0, 2]], [0, 1], [19, 19], 16, 3)
+    assert p.n_decode == 2
+
+
+def test_unused_table_entries_are_ignored(built_lib):
+    p = plan([5], [[2, -1, 77]], [0], [4], 16, 3)
+    assert p.queries == 1
+
+
+def test_work_lists_split_runs_into_tiles(built_lib):
+    # sequence 0: a 300-query prefill run; sequence 1: a 10-query run (decode items);
+    # sequence 2: one decode query
+    q_seq = [0] * 300 + [1] * 10 + [2]
+    q_pos = list(range(100, 400)) + list(range(50, 60)) + [7]
+    p = plan([400, 60, 8], [[i for i in range(25)], [30 + i for i in range(25)], [60] + [0] * 24],
+             q_seq, q_pos, 16, 61)
+    assert p.n_tiles == 3 and p.n_tile_queries == 300      # 128 + 128 + 44
+    assert p.n_decode == 11
+
+
+def test_empty_plan(built_lib):
+    p = plan([], np.zeros((0, 0), dtype=np.int32), [], [], 16, 0)
+    assert p.queries == 0 and p.device_bytes() % 16 == 0
+
+
+def test_workspace_bytes(built_lib):
+    n = pka.workspace_bytes(4, 64, 128, 64)
+    assert n == ((64 * 4 * 64 * 128 * 4 + 255) // 256 * 256) + ((64 * 4 * 64 * 4 + 255) // 256 * 256)
+    assert pka.workspace_bytes(4, 0, 128, 2) == 0
+    assert pka.workspace_bytes(4, 64, 128, 0) == 0
+
+
+def test_split_heuristic(built_lib):
+    lens = [32768, 65536, 98304, 131072]
+    table = np.arange(sum(n // 16 for n in lens), dtype=np.int32)
+    rows, off = [], 0
+    for n in lens:
+        rows.append(np.pad(table[off:off + n // 16], (0, 8192 - n // 16)))
+        off += n // 16
+    p = plan(lens, np.stack(rows), [0, 1, 2, 3], [n - 1 for n in lens], 16, int(table.size))
+    s = pka.paged_attn_split_heuristic(p, 64, 8, num_sms=152)
+    assert 8 <= s <= 64
+    small = plan([20], [[0, 1]], [0], [19], 16, 2)
+    assert pka.paged_attn_split_heuristic(small, 8, 8, num_sms=152) == 1   # one page: no split
+
+
+def _lib():
+    return pka.load()
+
+
+def test_attention_argument_checks_before_launch(built_lib):
+    """Bad heads, dims, scale, splits or workspace are refused with no device work."""
+    lib = _lib()
+    p = plan([5], [[0]], [0], [4], 16, 1)
+    h = p.handle
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails validation first
+    f = lib.paged_attn_forward
+    assert f(h, fake, fake, fake, fake, 6, 4, 64, 64, 0.1, 1, 2, None) == 2          # Hq % Hkv
+    assert f(h, fake, fake, fake, fake, 0, 1, 64, 64, 0.1, 1, 2, None) == 2          # Hq == 0
+    assert f(h, fake, fake, fake, fake, 4, 4, 1025, 64, 0.1, 1, 2, None) == 8        # d > 1024
+    assert f(h, fake, fake, fake, fake, 4, 4, 64, 0, 0.1, 1, 2, None) == 2           # dv == 0
+    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, float("nan"), 1, 2, None) == 2  # scale NaN
+    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, -1.0, 1, 2, None) == 2         # scale <= 0
+    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 7, None) == 3          # dtype
+    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, None) == 10         # not uploaded
+    fs = lib.paged_attn_forward_split
+    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, fake, 1 << 20, 65, None) == 7
+    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, fake, 1 << 20, 0, None) == 7
+    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, fake, 16, 4, None) == 6   # too small
+    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, None, 1 << 20, 4, None) == 6
+    m = lib.paged_mla_forward
+    assert m(h, fake, fake, fake, fake, fake, 4, 64, 0, 0.1, 1, 2, None, 0, 1, None) == 8     # P == 0
+    assert m(h, fake, fake, fake, fake, fake, 4, 64, 257, 0.1, 1, 2, None, 0, 1, None) == 8   # P > 256
+    assert m(h, fake, fake, fake, fake, fake, 4, 64, 64, 0.1, 1, 2, None, 0, 2, None) == 7    # split w/o ws
+    st = lib.paged_kv_store
+    assert st(h, fake, fake, fake, fake, 0, 64, 64, 2, None) == 2
+    assert st(h, fake, fake, fake, fake, 1, 64, 64, 9, None) == 3
+    assert st(h, fake, fake, fake, fake, 1, 64, 64, 2, None) == 10                     # not uploaded
+    assert st(None, fake, fake, fake, fake, 1, 64, 64, 2, None) == 1
+    assert lib.pa_last_error().decode().startswith("paged_kv_store")
+
+
+def test_zero_queries_is_ok_without_launch(built_lib):
+    lib = _lib()
+    p = plan([5], [[0]], [], [], 16, 1)
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.paged_attn_forward(p.handle, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, None) == 0
+    assert lib.paged_kv_store(p.handle, fake, fake, fake, fake, 1, 64, 64, 2, None) == 0
