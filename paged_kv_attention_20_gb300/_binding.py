@@ -16,7 +16,7 @@ import os
 import numpy as np
 import torch
 
-from . import build as _build
+from . import buildlib as _build
 
 _LIB = None
 
@@ -52,7 +52,7 @@ def load() -> ctypes.CDLL:
         return _LIB
     path = lib_path()
     if not os.path.exists(path):
-        raise RuntimeError(f"{path} is missing: build it with paged_kv_attention_20_gb300.build.build() "
+        raise RuntimeError(f"{path} is missing: build it with paged_kv_attention_20_gb300.build() "
                            "(nvcc, sm_103a); there is no fallback path")
     lib = ctypes.CDLL(path)
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t

@@ -2,7 +2,7 @@
 
 Every translation unit under csrc/ is compiled in parallel into _build/ and
 linked into paged_kv_attention_20_gb300/libpagedattn.so (static CUDA runtime).
-Run ``python -m paged_kv_attention_20_gb300.build`` or call ``build()``.
+Run ``python -m paged_kv_attention_20_gb300.buildlib`` or call ``build()``.
 """
 from __future__ import annotations
 
@@ -69,15 +69,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
     tmp = LIB + f".{os.getpid()}.tmp"
-    cmd = [cc, "-shared"] + ARCH + ["-o", tmp] + objs + ["-lcuda"]
+    cmd = [cc, "-shared"] + ARCH + ["-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        # libcuda is only needed for the driver entry points the tensor-map code resolves
-        # at run time; link without it when no stub is available.
-        cmd = [c for c in cmd if c != "-lcuda"]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"link failed:\n{r.stderr}")
+        raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
     return LIB
 
