@@ -46,6 +46,7 @@ struct AttnArgs {
     int32_t causal;
     int32_t splits;
     pa_dtype dtype;
+    int32_t *status;      // device status word (bounded waits record timeouts here)
 };
 
 // Launchers (return cudaGetLastError() of the launch).
@@ -63,5 +64,7 @@ cudaError_t launch_mla(const AttnArgs &a, bool use_decode_list, cudaStream_t st)
 
 // Device status word (bounded waits record their timeouts here).
 cudaError_t read_device_status(int32_t *code, bool clear);
+// Device address of the status word on the current device (cached per device).
+int32_t *device_status_ptr();
 
 }  // namespace pa

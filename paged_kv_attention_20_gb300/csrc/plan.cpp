@@ -172,6 +172,18 @@ pa_status paged_attn_plan(const int32_t *seq_lens, int32_t num_seqs, const int32
     }
     p->n_decode = (int32_t)decode.size();
     p->n_tiles = (int32_t)(tiles.size() / 4);
+    {
+        // Heaviest tiles first (most keys: largest last position), so the
+        // tensor-core kernel's long CTAs start early and the tail is short.
+        std::vector<int> order((size_t)p->n_tiles);
+        for (int t = 0; t < p->n_tiles; ++t) order[(size_t)t] = t;
+        auto last_pos = [&](int t) { return tiles[4 * (size_t)t + 3] + tiles[4 * (size_t)t + 2] - 1; };
+        std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return last_pos(a) > last_pos(b); });
+        std::vector<int32_t> sorted;
+        sorted.reserve(tiles.size());
+        for (int t : order) sorted.insert(sorted.end(), tiles.begin() + 4 * t, tiles.begin() + 4 * t + 4);
+        tiles.swap(sorted);
+    }
 
     // Word layout (int32 words; 16-byte aligned sections):
     //   [0..15]  header: magic, queries, sequences, width, page_size, pages,
@@ -322,6 +334,8 @@ pa_status attention(const pa_plan *plan, const void *q, const void *k, const voi
     a.q = q; a.k = k; a.v = v; a.qp = qp; a.kp = kp; a.out = out;
     a.hq = hq; a.hkv = hkv; a.d = d; a.dv = dv; a.p = mla ? p : 0;
     a.scale = scale; a.causal = causal; a.splits = splits; a.dtype = dtype;
+    a.status = pa::device_status_ptr();
+    if (!a.status) return bad(PA_ERR_CUDA, "device status word unavailable");
     if (splits > 1) {
         size_t rows = (size_t)splits * plan->queries * hq;
         a.ws_o = static_cast<float *>(ws);

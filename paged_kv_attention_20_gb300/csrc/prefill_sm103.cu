@@ -1,10 +1,412 @@
-// Chunked causal prefill on tcgen05 tensor cores (filled in below).
+// Chunked causal prefill on tcgen05 tensor cores.
+//
+// ruDNN 0.1.7, src/paged_attention/mod.rs: module doc ("packed decode and
+// chunked prefill") and `DevicePlan::attention` (causal at the plan's
+// absolute positions, prefill chunks included).  A chunk is a run of
+// consecutive positions of one sequence; query i of a chunk at position p_i
+// sees keys 0..p_i: the cached context plus the chunk's earlier rows.
+//
+// One CTA per (tile of up to 128 consecutive queries, query head):
+//   warps 0-3  softmax / O correction / epilogue, thread r owns query row r
+//              (TMEM lane r);
+//   warp 4     TMA producer: Q once, then K/V tiles of 128 keys gathered
+//              page by page through the block table (one 16-row box per
+//              page and 64-column half, 128-byte swizzle), 2-stage ring;
+//   warp 5     MMA issuer: S = Q K^T into one of two TMEM S buffers, then
+//              O += P V with P (bf16, written by the softmax warps in the
+//              swizzled K-major layout) in shared memory.
+// Key tiles past the last query's position are never loaded; the diagonal
+// tiles are masked per row.  Keys at or past the sequence length never reach
+// P.V: their scores are masked and their V rows are zeroed in shared memory
+// (tail slots may hold anything, NaN included).  The online softmax keeps a
+// per-row reference maximum that only moves when a tile's maximum exceeds it
+// by more than 8 (log2 units), so O in TMEM is rarely rescaled.
+// Every wait is bounded; a timeout sets the library's device status word and
+// the CTA stops issuing work.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "pa_internal.h"
+#include "sm103_tc.cuh"
 
 namespace pa {
+namespace {
 
-bool prefill_supported(const AttnArgs &) { return false; }
+using namespace tc;
 
-cudaError_t launch_prefill(const AttnArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kM = 128;          // queries per tile (TMEM lanes)
+constexpr int kN = 128;          // keys per tile
+constexpr int kD = 128;          // head dim (== value dim)
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr uint32_t kHalfBytes = kM * 128;          // one 64-column half of a 128-row tile
+constexpr uint32_t kTileBytes = 2 * kHalfBytes;    // 32 KB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kSlack = 8.f;
+
+struct Smem {
+    // 1024-byte aligned operand tiles (128-byte swizzle atoms)
+    uint8_t q[kTileBytes];
+    uint8_t k[kStages][kTileBytes];
+    uint8_t v[kStages][kTileBytes];
+    uint8_t p[kTileBytes];
+    uint64_t q_full;
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t s_full[2];
+    uint64_t s_free[2];
+    uint64_t p_ready;
+    uint64_t o_done;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+struct PrefillParams {
+    PlanView plan;
+    void *out;
+    int32_t *status;
+    int hq, hkv;
+    float scale_log2;
+    int causal;
+    int bf16;
+};
+
+__device__ __forceinline__ void set_timeout(Smem &s, int32_t *status, int code) {
+    atomicExch(&s.abort, 1);
+    atomicCAS(status, 0, code);
+}
+
+template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, PrefillParams prm) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // Heaviest tiles first: the plan orders tiles by decreasing key count.
+    const int tile_idx = blockIdx.x / prm.hq;
+    const int h = blockIdx.x % prm.hq;
+    const int kvh = h / (prm.hq / prm.hkv);
+    const int4 tile = prm.plan.tiles[tile_idx];
+    const int seq = tile.x, q0 = tile.y, nq = tile.z, pos0 = tile.w;
+    const int ps = prm.plan.page_size;
+    const int seq_len = prm.plan.seq_lens[seq];
+    const int last_pos = pos0 + nq - 1;
+    const int n_keys = prm.causal ? last_pos + 1 : seq_len;
+    const int n_kt = (n_keys + kN - 1) / kN;
+    const int32_t *trow = prm.plan.table + (int64_t)seq * prm.plan.width;
+
+    if (tid == 0) {
+        mbar_init(&s.q_full, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&s.kv_full[i], 1);
+            mbar_init(&s.kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.s_full[i], 1);
+            mbar_init(&s.s_free[i], kM);
+        }
+        mbar_init(&s.p_ready, kM);
+        mbar_init(&s.o_done, 1);
+        s.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+    const uint32_t tmem_s[2] = {tmem, tmem + 128};
+    const uint32_t tmem_o = tmem + 256;
+
+    if (warp == 4) {
+        // ---------------------------------------------------- TMA producer --
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(&s.q_full, kTileBytes);
+            tma_load_3d(s.q, &tm_q, 0, h, q0, &s.q_full);
+            tma_load_3d(s.q + kHalfBytes, &tm_q, 64, h, q0, &s.q_full);
+            const int oob_row = prm.plan.pages * ps;          // rows >= this read as zeros
+            const int used_pages = (seq_len + ps - 1) / ps;
+            for (int kt = 0; kt < n_kt; ++kt) {
+                const int st = kt % kStages;
+                if (kt >= kStages && !mbar_wait(&s.kv_empty[st], ((kt / kStages) - 1) & 1)) {
+                    set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
+                    break;
+                }
+                if (s.abort) break;
+                mbar_arrive_expect_tx(&s.kv_full[st], 2 * kTileBytes);
+                const int pages_per_tile = kN / ps;
+                for (int i = 0; i < pages_per_tile; ++i) {
+                    const int lp = kt * pages_per_tile + i;
+                    const int row = lp < used_pages ? trow[lp] * ps : oob_row;
+                    const uint32_t off = (uint32_t)i * ps * 128;
+                    tma_load_3d(s.k[st] + off, &tm_k, 0, kvh, row, &s.kv_full[st]);
+                    tma_load_3d(s.k[st] + kHalfBytes + off, &tm_k, 64, kvh, row, &s.kv_full[st]);
+                    tma_load_3d(s.v[st] + off, &tm_v, 0, kvh, row, &s.kv_full[st]);
+                    tma_load_3d(s.v[st] + kHalfBytes + off, &tm_v, 64, kvh, row, &s.kv_full[st]);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------ MMA issuer --
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16(kM, kN, prm.bf16 != 0, false, false);
+            const uint32_t idesc_o = idesc_f16(kM, kD, prm.bf16 != 0, false, true);
+            const uint32_t q_addr = smem_u32(s.q), p_addr = smem_u32(s.p);
+            bool ok = mbar_wait(&s.q_full, 0);
+            auto issue_pv = [&](int kt) -> bool {
+                if (!mbar_wait(&s.p_ready, kt & 1)) return false;
+                tc_fence_after();
+                const int st = kt % kStages;
+                const uint32_t v_addr = smem_u32(s.v[st]);
+                for (int ks = 0; ks < kN / 16; ++ks) {
+                    const uint64_t a = smem_desc(p_addr + (ks / 4) * kHalfBytes + (ks % 4) * 32, 16, 1024,
+                                                 kLayoutSwizzle128B);
+                    const uint64_t b = smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, kLayoutSwizzle128B);
+                    mma_f16_ss(tmem_o, a, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
+                }
+                mma_commit(&s.o_done);
+                mma_commit(&s.kv_empty[st]);
+                return true;
+            };
+            for (int kt = 0; ok && kt < n_kt; ++kt) {
+                const int st = kt % kStages, sb = kt & 1;
+                if (!mbar_wait(&s.kv_full[st], (kt / kStages) & 1)) { ok = false; break; }
+                if (kt >= 2 && !mbar_wait(&s.s_free[sb], ((kt / 2) - 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t k_addr = smem_u32(s.k[st]);
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t o = (ks / 4) * kHalfBytes + (ks % 4) * 32;
+                    mma_f16_ss(tmem_s[sb], smem_desc(q_addr + o, 16, 1024, kLayoutSwizzle128B),
+                               smem_desc(k_addr + o, 16, 1024, kLayoutSwizzle128B), idesc_s, ks > 0 ? 1u : 0u);
+                }
+                mma_commit(&s.s_full[sb]);
+                if (kt > 0 && !issue_pv(kt - 1)) { ok = false; break; }
+            }
+            if (ok && n_kt > 0) ok = issue_pv(n_kt - 1);
+            if (!ok) set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_MMA);
+        }
+    } else {
+        // ---------------------------------------- softmax / correction rows --
+        const int r = tid;                       // query row == TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        const int my_pos = pos0 + r;
+        const int vis_end = prm.causal ? min(my_pos + 1, seq_len) : seq_len;  // keys [0, vis_end)
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int kt = 0; kt < n_kt && ok; ++kt) {
+            const int sb = kt & 1;
+            if (!mbar_wait(&s.s_full[sb], (kt / 2) & 1)) { ok = false; break; }
+            tc_fence_after();
+            const int kbase = kt * kN;
+            // pass 1: tile max over visible keys
+            float mt = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < kN; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem_s[sb] + lane_off + c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (kbase + c + i < vis_end) mt = fmaxf(mt, __uint_as_float(v[i]) * prm.scale_log2);
+            }
+            float alpha = 1.f;
+            if (mt > m_ref + kSlack) {
+                alpha = exp2f(m_ref - mt);
+                m_ref = mt;
+            }
+            // the previous P.V must be done before P is overwritten or O rescaled
+            if (kt > 0 && !mbar_wait(&s.o_done, (kt - 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            if (alpha != 1.f && kt > 0) {
+#pragma unroll 1
+                for (int c = 0; c < kD; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tmem_o + lane_off + c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                    tmem_st16(tmem_o + lane_off + c, v);
+                }
+                tmem_wait_st();
+            }
+            // pass 2: P = exp2(s - m_ref) as 16-bit, written in the swizzled K-major layout
+            float lsum = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < kN; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem_s[sb] + lane_off + c, v);
+                tmem_wait_ld();
+                float p[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const bool vis = kbase + c + i < vis_end;
+                    p[i] = vis ? exp2f(__uint_as_float(v[i]) * prm.scale_log2 - m_ref) : 0.f;
+                    lsum += p[i];
+                }
+                uint4 w0, w1;
+                w0.x = pack2<T>(p[0], p[1]);   w0.y = pack2<T>(p[2], p[3]);
+                w0.z = pack2<T>(p[4], p[5]);   w0.w = pack2<T>(p[6], p[7]);
+                w1.x = pack2<T>(p[8], p[9]);   w1.y = pack2<T>(p[10], p[11]);
+                w1.z = pack2<T>(p[12], p[13]); w1.w = pack2<T>(p[14], p[15]);
+                const int half = c / 64, chunk = (c % 64) / 8;  // two 16-byte chunks per 16 keys
+                uint8_t *row = s.p + half * kHalfBytes + r * 128;
+                *reinterpret_cast<uint4 *>(row + (((chunk) ^ (r & 7)) * 16)) = w0;
+                *reinterpret_cast<uint4 *>(row + (((chunk + 1) ^ (r & 7)) * 16)) = w1;
+            }
+            tc_fence_before();
+            mbar_arrive(&s.s_free[sb]);
+            l = l * alpha + lsum;
+            // V rows at or past the sequence end (tail slots) must not reach the MMA
+            if (kbase + kN > seq_len) {
+                const int st = kt % kStages;
+                if (!mbar_wait(&s.kv_full[st], (kt / kStages) & 1)) { ok = false; break; }
+                if (kbase + r >= seq_len) {
+                    uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        *reinterpret_cast<uint4 *>(s.v[st] + r * 128 + i * 16) = z;
+                        *reinterpret_cast<uint4 *>(s.v[st] + kHalfBytes + r * 128 + i * 16) = z;
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&s.p_ready);
+        }
+        if (ok && n_kt > 0 && !mbar_wait(&s.o_done, (n_kt - 1) & 1)) ok = false;
+        if (!ok) {
+            set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_SOFTMAX);
+        } else if (r < nq) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            T *dst = static_cast<T *>(prm.out) + ((int64_t)(q0 + r) * prm.hq + h) * kD;
+#pragma unroll 1
+            for (int c = 0; c < kD; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem_o + lane_off + c, v);
+                tmem_wait_ld();
+                uint4 w0, w1;
+                w0.x = pack2<T>(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
+                w0.y = pack2<T>(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+                w0.z = pack2<T>(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
+                w0.w = pack2<T>(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
+                w1.x = pack2<T>(__uint_as_float(v[8]) * inv, __uint_as_float(v[9]) * inv);
+                w1.y = pack2<T>(__uint_as_float(v[10]) * inv, __uint_as_float(v[11]) * inv);
+                w1.z = pack2<T>(__uint_as_float(v[12]) * inv, __uint_as_float(v[13]) * inv);
+                w1.w = pack2<T>(__uint_as_float(v[14]) * inv, __uint_as_float(v[15]) * inv);
+                reinterpret_cast<uint4 *>(dst + c)[0] = w0;
+                reinterpret_cast<uint4 *>(dst + c)[1] = w1;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 3-D map over [rows, heads, 128] 16-bit elements; box = 64 columns x 1 head x box_rows rows.
+bool make_map(CUtensorMap *m, const void *base, int heads, int64_t rows, int box_rows, bool bf16) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * 2 * heads};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+bool prefill_supported(const AttnArgs &a) {
+    const int ps = a.plan.page_size;
+    return (a.dtype == PA_BF16 || a.dtype == PA_F16) && a.p == 0 && a.d == kD && a.dv == kD &&
+           (ps == 16 || ps == 32 || ps == 64 || ps == 128) && aligned16(a.q) && aligned16(a.k) &&
+           aligned16(a.v) && aligned16(a.out) && a.plan.n_tiles > 0 && encoder() != nullptr;
+}
+
+cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {
+    const bool bf16 = a.dtype == PA_BF16;
+    CUtensorMap tq, tk, tv;
+    const int64_t cache_rows = (int64_t)a.plan.pages * a.plan.page_size;
+    if (!make_map(&tq, a.q, a.hq, a.plan.queries, kM, bf16) ||
+        !make_map(&tk, a.k, a.hkv, cache_rows, a.plan.page_size, bf16) ||
+        !make_map(&tv, a.v, a.hkv, cache_rows, a.plan.page_size, bf16))
+        return cudaErrorInvalidValue;
+    PrefillParams prm{};
+    prm.plan = a.plan;
+    prm.out = a.out;
+    prm.status = a.status;
+    prm.hq = a.hq;
+    prm.hkv = a.hkv;
+    prm.scale_log2 = a.scale * kLog2e;
+    prm.causal = a.causal;
+    prm.bf16 = bf16 ? 1 : 0;
+    const dim3 grid((unsigned)(a.plan.n_tiles * a.hq));
+    cudaError_t e;
+    if (bf16) {
+        static bool cfg = false;
+        if (!cfg) {
+            e = cudaFuncSetAttribute(prefill_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
+            if (e != cudaSuccess) return e;
+            cfg = true;
+        }
+        prefill_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, prm);
+    } else {
+        static bool cfg = false;
+        if (!cfg) {
+            e = cudaFuncSetAttribute(prefill_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
+            if (e != cudaSuccess) return e;
+            cfg = true;
+        }
+        prefill_kernel<__half><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, prm);
+    }
+    return cudaGetLastError();
+}
 
 }  // namespace pa

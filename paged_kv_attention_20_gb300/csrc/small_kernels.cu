@@ -123,6 +123,18 @@ cudaError_t launch_merge(const AttnArgs &a, bool use_list, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+int32_t *device_status_ptr() {
+    static int32_t *cached[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cached[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        cached[dev] = static_cast<int32_t *>(p);
+    }
+    return cached[dev];
+}
+
 cudaError_t read_device_status(int32_t *code, bool clear) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return e;
