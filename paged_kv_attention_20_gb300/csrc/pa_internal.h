@@ -54,6 +54,9 @@ struct AttnArgs {
 cudaError_t launch_kv_store(const PlanView &plan, const void *new_k, const void *new_v, void *k_cache,
                             void *v_cache, int heads, int d, int dv, int elem_bytes, cudaStream_t st);
 cudaError_t launch_decode(const AttnArgs &a, bool use_decode_list, cudaStream_t st);
+// Warp-independent TMA decode (bf16/f16, D == Dv in {64,128,256}, power-of-two pages).
+bool decode_tma_supported(const AttnArgs &a);
+cudaError_t launch_decode_tma(const AttnArgs &a, bool use_decode_list, cudaStream_t st);
 cudaError_t launch_merge(const AttnArgs &a, bool use_decode_list, cudaStream_t st);
 // Tensor-core prefill over plan.tiles; returns cudaErrorNotSupported when the
 // shape/dtype is outside what the kernel covers (caller then uses decode for all).
@@ -68,3 +71,6 @@ cudaError_t read_device_status(int32_t *code, bool clear);
 int32_t *device_status_ptr();
 
 }  // namespace pa
+
+// Record `msg` as this thread's last error and return `status`.
+pa_status pa_fail_with(pa_status status, const char *msg);

@@ -68,6 +68,8 @@ bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u
 
 }  // namespace
 
+pa_status pa_fail_with(pa_status status, const char *msg) { return fail(status, msg); }
+
 extern "C" {
 
 const char *pa_last_error(void) { return g_error.c_str(); }

@@ -25,12 +25,12 @@
 // the CTA stops issuing work.
 
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "pa_internal.h"
 #include "sm103_tc.cuh"
+#include "tma_host.h"
 
 namespace pa {
 namespace {
@@ -218,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int kt = 0; kt < n_kt && ok; ++kt) {
             const int sb = kt & 1;
-            if (!mbar_wait(&s.s_full[sb], (kt / 2) & 1)) { ok = false; break; }
+            ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[sb], (kt / 2) & 1));
+            if (!ok) break;
             tc_fence_after();
             const int kbase = kt * kN;
             // pass 1: tile max over visible keys
@@ -238,9 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = mt;
             }
             // the previous P.V must be done before P is overwritten or O rescaled
-            if (kt > 0 && !mbar_wait(&s.o_done, (kt - 1) & 1)) { ok = false; break; }
+            if (kt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done, (kt - 1) & 1));
+            if (!ok) break;
             tc_fence_after();
-            if (alpha != 1.f && kt > 0) {
+            // tcgen05.ld/st are warp-collective: the whole warp rescales when any row needs it
+            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                 for (int c = 0; c < kD; c += 16) {
                     uint32_t v[16];
@@ -282,7 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // V rows at or past the sequence end (tail slots) must not reach the MMA
             if (kbase + kN > seq_len) {
                 const int st = kt % kStages;
-                if (!mbar_wait(&s.kv_full[st], (kt / kStages) & 1)) { ok = false; break; }
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.kv_full[st], (kt / kStages) & 1));
+                if (!ok) break;
                 if (kbase + r >= seq_len) {
                     uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -295,10 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             mbar_arrive(&s.p_ready);
         }
-        if (ok && n_kt > 0 && !mbar_wait(&s.o_done, (n_kt - 1) & 1)) ok = false;
+        if (ok && n_kt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done, (n_kt - 1) & 1));
         if (!ok) {
             set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_SOFTMAX);
-        } else if (r < nq) {
+        } else {
+            // every lane loads (warp-collective); only rows of real queries store
             tc_fence_after();
             const float inv = 1.f / l;
             T *dst = static_cast<T *>(prm.out) + ((int64_t)(q0 + r) * prm.hq + h) * kD;
@@ -316,8 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 w1.y = pack2<T>(__uint_as_float(v[10]) * inv, __uint_as_float(v[11]) * inv);
                 w1.z = pack2<T>(__uint_as_float(v[12]) * inv, __uint_as_float(v[13]) * inv);
                 w1.w = pack2<T>(__uint_as_float(v[14]) * inv, __uint_as_float(v[15]) * inv);
-                reinterpret_cast<uint4 *>(dst + c)[0] = w0;
-                reinterpret_cast<uint4 *>(dst + c)[1] = w1;
+                if (r < nq) {
+                    reinterpret_cast<uint4 *>(dst + c)[0] = w0;
+                    reinterpret_cast<uint4 *>(dst + c)[1] = w1;
+                }
             }
         }
     }
@@ -329,32 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
 // 3-D map over [rows, heads, 128] 16-bit elements; box = 64 columns x 1 head x box_rows rows.
 bool make_map(CUtensorMap *m, const void *base, int heads, int64_t rows, int box_rows, bool bf16) {
-    auto enc = encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * 2 * heads};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                     const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_map_3d(m, base, bf16, kD, (uint64_t)heads, (uint64_t)rows, (uint64_t)kD * 2,
+                         (uint64_t)kD * 2 * heads, 64, 1, (uint32_t)box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -365,7 +350,7 @@ bool prefill_supported(const AttnArgs &a) {
     const int ps = a.plan.page_size;
     return (a.dtype == PA_BF16 || a.dtype == PA_F16) && a.p == 0 && a.d == kD && a.dv == kD &&
            (ps == 16 || ps == 32 || ps == 64 || ps == 128) && aligned16(a.q) && aligned16(a.k) &&
-           aligned16(a.v) && aligned16(a.out) && a.plan.n_tiles > 0 && encoder() != nullptr;
+           aligned16(a.v) && aligned16(a.out) && a.plan.n_tiles > 0 && tma_available();
 }
 
 cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {

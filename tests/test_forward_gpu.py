@@ -229,3 +229,60 @@ def test_repeat_calls_reuse_workspace_across_plans(cuda_device):
         out = pka.paged_attn_forward_split(plan, dc.q, dc.k_cache, dc.v_cache, case.scale, 8, workspace=ws)
         ref, _, _, _ = oracle_after_store(case)
         assert_close(out.cpu().double().numpy(), ref, case.dtype, case.name)
+
+
+# ------------------------------------------------ tensor-core paths (sm_103a) --
+
+def _sampled(case, nrows, seed, splits=None):
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(case.num_queries * case.hq, size=nrows, replace=False))
+    out, _, _, _ = gpu_store_and_attend(case, splits=splits)
+    ref, _, _, _ = oracle_after_store(case, rows=rows)
+    got = out.double().numpy().reshape(-1, case.dv)[rows]
+    return assert_close(got, ref, case.dtype, case.name)
+
+
+def test_mixed_prefill_decode_full_sampled(cuda_device):
+    """8 prefill chunks of 512 queries at offsets up to 4096 plus 120 decode queries."""
+    _sampled(mixed_prefill_decode_bf16(), 96, 4)
+
+
+def test_mla_decode_full_sampled(cuda_device):
+    """128 queries x 128 heads, latent 512 + position 64, contexts up to 16K, page size 64."""
+    _sampled(mla_decode_bf16(), 64, 5)
+
+
+@pytest.mark.parametrize("heads,ps,dtype", [(256, 64, torch.bfloat16), (128, 16, torch.bfloat16),
+                                            (100, 64, torch.float16), (128, 128, torch.bfloat16)])
+def test_mla_shapes(cuda_device, heads, ps, dtype):
+    case = mla_decode_bf16(num_seqs=4, heads=heads, ctx_lo=1, ctx_hi=600)
+    if ps != 64 or dtype != torch.bfloat16:
+        ctx = list(case.seq_lens)
+        case = build_case("mla_shapes", 31, ctx, decode_queries(ctx), heads, 1, 512, 64, ps, dtype,
+                          1 / math.sqrt(192), mla_p=64)
+    _compare(case, what=f"mla H={heads} ps={ps} {dtype}")
+
+
+def test_mla_non_causal_and_splits(cuda_device):
+    seq_lens = [70, 300, 129]
+    queries = [(0, 5), (1, 299), (2, 64)]
+    case = build_case("mla_nc", 32, seq_lens, queries, 128, 1, 512, 64, 64, torch.bfloat16,
+                      1 / math.sqrt(192), mla_p=64)
+    _compare(case, causal=False, what="mla non-causal")
+    for s in (2, 3, 8):
+        _compare(case, splits=s, what=f"mla split {s}")
+
+
+@pytest.mark.parametrize("ps,dtype", [(16, torch.bfloat16), (64, torch.bfloat16), (16, torch.float16),
+                                      (32, torch.bfloat16)])
+def test_prefill_chunks(cuda_device, ps, dtype):
+    """Chunks at offset 0 and mid-sequence, run lengths that leave partial 128-query tiles."""
+    seq_lens = [300, 700, 129, 40]
+    queries = [(0, i) for i in range(300)]                       # whole sequence from position 0
+    queries += [(1, 400 + i) for i in range(200)]                # mid-sequence chunk, partial tile
+    queries += [(2, 128 + 0)]                                    # decode query
+    queries += [(3, 20 + i) for i in range(20)]                  # short run (still a tile: >= 16)
+    case = build_case("prefill", 33, seq_lens, queries, 16, 4, 128, 128, ps, dtype, 1 / math.sqrt(128))
+    _compare(case, what=f"prefill ps={ps} {dtype}")
+    _compare(case, causal=False, what=f"prefill non-causal ps={ps}")
+    _compare(case, splits=4, what=f"prefill + split decode ps={ps}")
