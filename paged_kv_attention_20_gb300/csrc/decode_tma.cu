@@ -70,7 +70,7 @@ __device__ __forceinline__ void split_bounds(int64_t n, int splits, int s, int p
 template <int D, int GH>
 struct Cfg {
     static constexpr int NW = 4;                               // warps per CTA
-    static constexpr int NST = 3;                              // ring stages per warp
+    static constexpr int NST = 2;                              // ring stages per warp
     static constexpr int TT = 16;                              // tokens per tile
     static constexpr int DPL = (GH <= 4 && D >= 128) ? 16 : 8; // dims per lane (scores)
     static constexpr int SUB = DPL / 8;                        // 16-byte chunks per lane
@@ -82,7 +82,7 @@ struct Cfg {
     static constexpr int TILE = TT * ROW;                      // bytes of one K (or V) tile
     static constexpr int STAGE = 2 * TILE;
     static constexpr int WARP_RING = NST * STAGE;
-    static constexpr int SP = TT * GH;                         // per-warp score floats
+    static constexpr int SP = 3 * TT * GH;                     // per-warp: weight pairs [2*TT*GH] + scores [TT*GH]
     // shared layout: [rings NW*WARP_RING][scores NW*SP][alpha NW*8][barriers NW*NST]
     static constexpr size_t RINGS = (size_t)NW * WARP_RING;
     static constexpr size_t MERGE = (size_t)NW * GH * (D + 2) * 4;  // final warp merge (reuses rings)
@@ -139,15 +139,20 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BIG + (size_t)C::NW * C::SP * 4 + C::NW * 8 * 4) +
                      warp * C::NST;
 
-    const int item = blockIdx.x;
+    // Flattened grid, item slowest: the plan lists decode items longest first,
+    // so the heaviest (query, KV head, split) blocks start first.
+    const int hg_count = a.hkv * tp.groups;
+    const int hg = blockIdx.x % hg_count;
+    const int rest = blockIdx.x / hg_count;
+    const int split = rest % a.splits;
+    const int item = rest / a.splits;
     const int qi = use_list ? a.plan.decode[item] : item;
     const int4 meta = a.plan.qmeta[qi];
     const int seq = meta.x, pos = meta.y;
     const int ps = a.plan.page_size;
     const int64_t n = a.causal ? (int64_t)pos + 1 : (int64_t)a.plan.seq_lens[seq];
-    const int kvh = blockIdx.y / tp.groups;
-    const int h0 = kvh * (a.hq / a.hkv) + (blockIdx.y % tp.groups) * GH;
-    const int split = blockIdx.z;
+    const int kvh = hg / tp.groups;
+    const int h0 = kvh * (a.hq / a.hkv) + (hg % tp.groups) * GH;
     int64_t j0, j1;
     split_bounds(n, a.splits, split, ps, j0, j1);
     const int ntiles = (int)((j1 - j0 + C::TT - 1) / C::TT);
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
             int head;
             bool writer;
             const float s = reduce_heads<GH, C::LPT>(part, glane, head, writer);
-            if (writer) sp[t * GH + head] = s;
+            if (writer) sp[2 * C::TT * GH + t * GH + head] = s;
         }
         __syncwarp();
 
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
         for (int k = 0; k < HP; ++k) {
             const int g = 2 * k + (lane >> 4);
             const bool gv = g < GH;
-            const float s = (gv && t16 < valid) ? sp[t16 * GH + g] : -INFINITY;
+            const float s = (gv && t16 < valid) ? sp[2 * C::TT * GH + t16 * GH + g] : -INFINITY;
             float mt = s;
 #pragma unroll
             for (int o = 8; o; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
@@ -273,7 +278,7 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
             l_run[k] = l_run[k] * alpha + psum;
             m_ref[k] = nref;
             if (gv) {
-                sp[t16 * GH + g] = p;
+                reinterpret_cast<float2 *>(sp)[t16 * GH + g] = make_float2(p, p);
                 if (t16 == 0) al[g] = alpha;
             }
         }
@@ -299,22 +304,22 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
             } else {
                 vw[0] = *reinterpret_cast<const uint32_t *>(V + t * C::ROW + lane * 4);
             }
-            float pg[GH];
-            if constexpr (GH >= 4) {
+            float2 pg[GH];   // {p, p} pairs written by the softmax
+            if constexpr (GH >= 2) {
 #pragma unroll
-                for (int g4 = 0; g4 < GH / 4; ++g4) {
-                    const float4 w4 = reinterpret_cast<const float4 *>(sp + t * GH)[g4];
-                    pg[4 * g4] = w4.x; pg[4 * g4 + 1] = w4.y; pg[4 * g4 + 2] = w4.z; pg[4 * g4 + 3] = w4.w;
+                for (int g2 = 0; g2 < GH / 2; ++g2) {
+                    const float4 w4 = reinterpret_cast<const float4 *>(sp + 2 * t * GH)[g2];
+                    pg[2 * g2] = make_float2(w4.x, w4.y);
+                    pg[2 * g2 + 1] = make_float2(w4.z, w4.w);
                 }
             } else {
-#pragma unroll
-                for (int g = 0; g < GH; ++g) pg[g] = sp[t * GH + g];
+                pg[0] = reinterpret_cast<const float2 *>(sp)[t];
             }
 #pragma unroll
             for (int c = 0; c < C::CPL / 2; ++c) {
                 const float2 vf = unpack2<T>(vw[c]);
 #pragma unroll
-                for (int g = 0; g < GH; ++g) acc[g][c] = ffma2(make_float2(pg[g], pg[g]), vf, acc[g][c]);
+                for (int g = 0; g < GH; ++g) acc[g][c] = ffma2(pg[g], vf, acc[g][c]);
             }
         }
         __syncwarp();
@@ -391,7 +396,7 @@ cudaError_t launch_t(const AttnArgs &a, int items, int use_list, const CUtensorM
     }
     TmaParams p = tp;
     p.groups = (a.hq / a.hkv) / GH;
-    dim3 grid(items, a.hkv * p.groups, a.splits);
+    const dim3 grid((unsigned)((int64_t)items * a.splits * a.hkv * p.groups));
     decode_tma_kernel<T, D, GH><<<grid, 128, C::SMEM, st>>>(tk, tv, a, use_list, p);
     return cudaGetLastError();
 }

@@ -172,6 +172,10 @@ pa_status paged_attn_plan(const int32_t *seq_lens, int32_t num_seqs, const int32
         }
         i = j;
     }
+    // Longest decode items first (visible keys of a causal query: pos + 1), so
+    // the decode kernels' heaviest blocks start first.
+    std::stable_sort(decode.begin(), decode.end(),
+                     [&](int32_t a, int32_t b) { return query_pos[a] > query_pos[b]; });
     p->n_decode = (int32_t)decode.size();
     p->n_tiles = (int32_t)(tiles.size() / 4);
     {
@@ -358,8 +362,10 @@ pa_status attention(const pa_plan *plan, const void *q, const void *k, const voi
                 if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, true, st);
             }
         } else {
-            e = pa::launch_decode(a, false, st);
-            if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, false, st);
+            // every query is a decode item: use the (longest-first) decode list
+            const bool all_decode = plan->n_tiles == 0;
+            e = pa::launch_decode(a, all_decode, st);
+            if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, all_decode, st);
         }
     }
     if (e != cudaSuccess) return fail_cuda(e, name);
