@@ -230,6 +230,33 @@ pa_status paged_mla_forward(const pa_plan *plan, const void *q, const void *qp,
                             size_t workspace_bytes, int32_t splits, pa_stream_t stream);
 
 /*
+ * Split-KV forward that allocates nothing.  The pages have no counterpart for
+ * this call; it serves callers that cannot hand the library a workspace --
+ * code inside a host runtime that owns every device allocation (a serving
+ * engine with one fixed memory pool, a plugin host that forbids stray
+ * allocations) or that cannot afford cudaMalloc's implicit device-wide
+ * synchronisation in a decode loop.  Same arguments, checks and result as
+ * paged_attn_forward_split, but the split partials live in a file-scope device
+ * array of PA_STATIC_SCRATCH_BYTES that every GPU loading the library holds
+ * until the process exits.  The caller still owns q, the caches and out.
+ *
+ * Rejects (PA_ERR_WORKSPACE) any plan/heads/value_dim/splits whose
+ * pa_workspace_bytes exceeds PA_STATIC_SCRATCH_BYTES.  Calls no cudaMalloc,
+ * cudaFree or allocating library routine.  The first call on a device looks up
+ * the array's device address with that device current; make it before any
+ * stream capture.  All calls share the array and it keeps the last call's
+ * contents (each call writes every entry it later reads, so nothing needs
+ * clearing); calls whose GPU work overlaps race on it -- serialise them on one
+ * stream.
+ */
+#define PA_STATIC_SCRATCH_BYTES (16u << 20)
+pa_status paged_attn_forward_split_static(const pa_plan *plan, const void *q, const void *k_cache,
+                                          const void *v_cache, void *out, int32_t num_heads,
+                                          int32_t num_kv_heads, int32_t head_dim, int32_t value_dim,
+                                          float scale, int32_t causal, pa_dtype dtype, int32_t splits,
+                                          pa_stream_t stream);
+
+/*
  * Device-side status word.  Kernels that wait on hardware (mbarriers, tensor
  * memory) bound every wait; a wait that runs out sets this word to a non-zero
  * code (PA_DEVICE_TIMEOUT_*) and the kernel returns early, leaving the context
