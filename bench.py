@@ -192,7 +192,12 @@ class DecodeStep:
         self.plan = pka.paged_attn_plan(case.seq_lens, case.block_table, case.query_seq, case.query_pos,
                                         case.page_size, case.num_pages, device=device)
         sms = torch.cuda.get_device_properties(device).multi_processor_count
-        self.splits = splits or pka.paged_attn_split_heuristic(self.plan, case.hq, case.hkv, sms)
+        if splits:
+            self.splits = splits
+        elif case.is_mla:
+            self.splits = pka.paged_mla_split_heuristic(self.plan, case.hq, sms)
+        else:
+            self.splits = pka.paged_attn_split_heuristic(self.plan, case.hq, case.hkv, sms)
         self.ws = pka.make_workspace(self.plan, case.hq, case.dv, max(self.splits, 1), device)
         self.out = torch.empty(case.num_queries, case.hq, case.dv, dtype=case.dtype, device=device)
 
@@ -468,8 +473,9 @@ def main():
     value = world * kvb * args.steps / (total_ms / 1e3) / 1e9
     attn_mean = statistics.mean(attn_ms)
     achieved = kvb / (attn_mean / 1e3) / 1e9
-    traffic = profile_traffic("decode_fast_gqa_decode_bf16",
-                              ["paged_kv_attention_20_gb300/csrc/decode.cu"])
+    traffic = profile_traffic("decode_tma_gqa_decode_bf16",
+                              ["paged_kv_attention_20_gb300/csrc/decode_tma.cu",
+                               "paged_kv_attention_20_gb300/csrc/small_kernels.cu"])
 
     if rank != 0:
         barrier(world)
@@ -489,7 +495,7 @@ def main():
         "kernel_ms": {"store": statistics.mean(store_ms), "attention": attn_mean},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "decode_fast_kernel<bf16,128,4> (+ merge when splits > 1)",
+                     "kernel": "decode_tma_kernel<bf16,128,4> (+ merge_kernel when splits > 1)",
                      "peak_source": f"{peaks['source']} HBM copy bandwidth"},
         "clocks": clocks,
         "gpu_launches": args.steps * step.kernels_per_step(),

@@ -151,6 +151,14 @@ int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32
                                    int32_t num_sms);
 
 /*
+ * Split count for paged_mla_forward (same source as above; the rule is ours):
+ * the tensor-core MLA kernel runs one CTA pair per (query, 128 heads, split);
+ * aim for about two waves over `num_sms` SMs, each split keeping at least 256
+ * keys of the longest history, 1..PA_MAX_SPLITS.
+ */
+int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t num_sms);
+
+/*
  * Cache append (`DevicePlan::append_with_report`): for every query q and head
  * h, new_k[q, h, :] is copied bit-for-bit into k_cache[page, row, h, :] and
  * new_v[q, h, :] into v_cache[page, row, h, :], where page =

@@ -29,7 +29,7 @@ MAX_SPLITS = 64
 
 EXPORTED = ["pa_last_error", "pa_status_string", "pa_abi_version", "paged_attn_plan",
             "pa_plan_device_bytes", "pa_plan_upload", "pa_plan_destroy", "pa_plan_describe",
-            "pa_workspace_bytes", "paged_attn_split_heuristic", "paged_kv_store", "paged_attn_forward",
+            "pa_workspace_bytes", "paged_attn_split_heuristic", "paged_mla_split_heuristic", "paged_kv_store", "paged_attn_forward",
             "paged_attn_forward_split", "paged_mla_forward", "pa_device_status"]
 
 
@@ -74,6 +74,8 @@ def load() -> ctypes.CDLL:
     lib.pa_workspace_bytes.restype = sz
     lib.paged_attn_split_heuristic.argtypes = [vp, i32, i32, i32]
     lib.paged_attn_split_heuristic.restype = i32
+    lib.paged_mla_split_heuristic.argtypes = [vp, i32, i32]
+    lib.paged_mla_split_heuristic.restype = i32
     lib.paged_kv_store.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int, vp]
     lib.paged_kv_store.restype = ctypes.c_int
     lib.paged_attn_forward.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, i32,
@@ -219,6 +221,12 @@ def paged_attn_split_heuristic(plan: Plan, num_heads: int, num_kv_heads: int, nu
     if num_sms is None:
         num_sms = torch.cuda.get_device_properties(plan.device or 0).multi_processor_count
     return int(load().paged_attn_split_heuristic(plan.handle, int(num_heads), int(num_kv_heads), int(num_sms)))
+
+
+def paged_mla_split_heuristic(plan: Plan, num_heads: int, num_sms: int | None = None) -> int:
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(plan.device or 0).multi_processor_count
+    return int(load().paged_mla_split_heuristic(plan.handle, int(num_heads), int(num_sms)))
 
 
 def paged_kv_store(plan: Plan, new_k, new_v, k_cache, v_cache) -> None:

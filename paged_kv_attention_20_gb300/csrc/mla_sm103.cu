@@ -62,8 +62,8 @@ struct Smem {
     uint64_t s_free[2];
     uint64_t p_ready;
     uint64_t o_done;
-    uint64_t recv_full;                  // arrived by the peer's 128 threads after writing recv
-    uint64_t can_send;                   // arrived by the peer's 128 threads after reading its recv
+    uint64_t recv_full;                  // local expect_tx + the peer's asynchronous stores (bytes)
+    uint64_t can_send;                   // arrived by the peer's 4 row warps after reading its recv
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -102,9 +102,13 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t peer) {
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
+// Asynchronous store into the peer CTA's shared memory; its bytes complete a
+// transaction on the peer's mbarrier (no fence on the sending side).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(addr),
+        "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+        : "memory");
 }
 
 __device__ __forceinline__ void arrive_remote(uint32_t remote_bar) {
@@ -165,7 +169,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int rest = cl / prm.head_blocks;
     const int item = rest % (prm.use_list ? prm.plan.n_decode : prm.plan.queries);
     const int split = rest / (prm.use_list ? prm.plan.n_decode : prm.plan.queries);
-    const int qi = prm.use_list ? prm.plan.decode[item] : item;
+    const int qi = prm.use_list ? prm.plan.decode[item] : prm.plan.order[item];
     const int4 meta = prm.plan.qmeta[qi];
     const int seq = meta.x, pos = meta.y;
     const int ps = prm.plan.page_size;
@@ -188,8 +192,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_init(&s.p_ready, kHeads);
         mbar_init(&s.o_done, 1);
-        mbar_init(&s.recv_full, kHeads);
-        mbar_init(&s.can_send, kHeads);
+        mbar_init(&s.recv_full, 1);
+        mbar_init(&s.can_send, 4);
         s.abort = 0;
         fence_mbar_init();
     }
@@ -302,14 +306,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&s.s_free[sb]);
+            // this tile's receive: 128 rows x 64 floats from the peer
+            if (r == 0) mbar_arrive_expect_tx(&s.recv_full, kHeads * kN * 4);
             // send my partial to the peer (its buffer is free once it read the previous one)
             if (kt > 0) {
                 ok = __all_sync(0xffffffffu, wait_cluster(&s.can_send, (kt - 1) & 1));
                 if (!ok) break;
             }
 #pragma unroll
-            for (int c = 0; c < kN; c += 4) st_cluster_v4(recv_peer + c * 4, sc[c], sc[c + 1], sc[c + 2], sc[c + 3]);
-            arrive_remote(recv_full_peer);
+            for (int c = 0; c < kN; c += 4)
+                st_async_v4(recv_peer + c * 4, sc[c], sc[c + 1], sc[c + 2], sc[c + 3], recv_full_peer);
             ok = __all_sync(0xffffffffu, wait_cluster(&s.recv_full, kt & 1));
             if (!ok) break;
             const float *mine = &s.recv[r * kRecvStride];
@@ -318,7 +324,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float4 o = *reinterpret_cast<const float4 *>(mine + c);
                 sc[c] += o.x; sc[c + 1] += o.y; sc[c + 2] += o.z; sc[c + 3] += o.w;
             }
-            arrive_remote(can_send_peer);
+            __syncwarp();
+            if (lane == 0) arrive_remote(can_send_peer);   // this warp's rows are read
             // online softmax (identical on both CTAs)
             float mt = -INFINITY;
 #pragma unroll

@@ -21,6 +21,7 @@ struct PlanView {
     const int32_t *table;    // [sequences * width]
     const int32_t *decode;   // [n_decode] query indices handled by the decode kernel
     const int4 *tiles;       // [n_tiles] {seq, first query, query count, first position}
+    const int32_t *order;    // [queries] every query, longest visible history first
     int32_t queries;
     int32_t sequences;
     int32_t width;

@@ -23,7 +23,7 @@ struct pa_plan {
     int32_t n_decode = 0, n_tiles = 0, n_tile_queries = 0;
     int64_t max_seq_len = 0;          // longest sequence any decode item reads
     std::vector<int32_t> words;       // host copy of the device metadata
-    size_t off_qmeta = 0, off_seqlen = 0, off_table = 0, off_decode = 0, off_tiles = 0;
+    size_t off_qmeta = 0, off_seqlen = 0, off_table = 0, off_decode = 0, off_tiles = 0, off_order = 0;
     const int32_t *dev = nullptr;     // caller's device copy (after upload)
 };
 
@@ -54,6 +54,7 @@ pa::PlanView view_of(const pa_plan *p) {
     v.table = p->dev + p->off_table;
     v.decode = p->dev + p->off_decode;
     v.tiles = reinterpret_cast<const int4 *>(p->dev + p->off_tiles);
+    v.order = p->dev + p->off_order;
     v.queries = p->queries;
     v.sequences = p->sequences;
     v.width = p->width;
@@ -199,12 +200,14 @@ pa_status paged_attn_plan(const int32_t *seq_lens, int32_t num_seqs, const int32
     //   table    sequences x width
     //   decode   n_decode query indices
     //   tiles    n_tiles x {seq, first query, count, first position}
+    //   order    every query, longest visible history first
     size_t off = 16;
     p->off_qmeta = off;   off = align_words(off + 4 * (size_t)num_queries, 4);
     p->off_seqlen = off;  off = align_words(off + (size_t)num_seqs, 4);
     p->off_table = off;   off = align_words(off + (size_t)num_seqs * width, 4);
     p->off_decode = off;  off = align_words(off + decode.size(), 4);
     p->off_tiles = off;   off = align_words(off + tiles.size(), 4);
+    p->off_order = off;   off = align_words(off + (size_t)num_queries, 4);
     p->words.assign(off, 0);
     int32_t *w = p->words.data();
     w[0] = 0x50414731;  // "PAG1"
@@ -224,6 +227,13 @@ pa_status paged_attn_plan(const int32_t *seq_lens, int32_t num_seqs, const int32
         w[p->off_table + e] = block_table[e] < 0 ? 0 : block_table[e];  // unused entries never read
     if (!decode.empty()) std::memcpy(w + p->off_decode, decode.data(), sizeof(int32_t) * decode.size());
     if (!tiles.empty()) std::memcpy(w + p->off_tiles, tiles.data(), sizeof(int32_t) * tiles.size());
+    {
+        std::vector<int32_t> order((size_t)num_queries);
+        for (int32_t q = 0; q < num_queries; ++q) order[(size_t)q] = q;
+        std::stable_sort(order.begin(), order.end(),
+                         [&](int32_t a, int32_t b) { return query_pos[a] > query_pos[b]; });
+        if (num_queries) std::memcpy(w + p->off_order, order.data(), sizeof(int32_t) * order.size());
+    }
     *out_plan = p;
     return PA_OK;
 }
@@ -271,6 +281,19 @@ int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32
     int64_t cap = std::max<int64_t>(1, plan->max_seq_len / (4 * (int64_t)plan->page_size));
     s = std::min<int64_t>(s, cap);
     s = std::max<int64_t>(1, std::min<int64_t>(s, PA_MAX_SPLITS));
+    return (int32_t)s;
+}
+
+int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t num_sms) {
+    if (!plan || num_heads < 1 || num_sms < 1 || plan->queries == 0) return 1;
+    // one CTA pair per (query, 128 heads, split); aim for about two waves of SMs
+    const int64_t pairs = (int64_t)plan->queries * ((num_heads + 127) / 128);
+    int64_t s = (2 * (int64_t)num_sms + 2 * pairs - 1) / (2 * pairs);
+    int64_t longest = 0;
+    for (int32_t q = 0; q < plan->queries; ++q)
+        longest = std::max<int64_t>(longest, (int64_t)plan->words[plan->off_qmeta + 4 * (size_t)q + 1] + 1);
+    const int64_t cap = std::max<int64_t>(1, longest / 256);   // splits of at least 4 tiles of 64 keys
+    s = std::max<int64_t>(1, std::min<int64_t>(std::min(s, cap), PA_MAX_SPLITS));
     return (int32_t)s;
 }
 
