@@ -225,7 +225,10 @@ def time_step(step: DecodeStep, steps: int, warmup: int, world: int, device, sam
         step.store()
         step.attend()
     torch.cuda.synchronize(device)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    for e in evs:              # create the CUDA events before timing
+        for ev in e:
+            ev.record()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(device)
@@ -236,6 +239,7 @@ def time_step(step: DecodeStep, steps: int, warmup: int, world: int, device, sam
         evs[i][0].record()
         step.store()
         evs[i][1].record()
+        step.pka.time_next_kernel(evs[i][3], evs[i][4])   # brackets the main attention kernel
         step.attend()
         evs[i][2].record()
     t1.record()
@@ -245,7 +249,8 @@ def time_step(step: DecodeStep, steps: int, warmup: int, world: int, device, sam
     total = t0.elapsed_time(t1)
     store_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    return total, store_ms, attn_ms, clocks
+    kern_ms = [e[3].elapsed_time(e[4]) for e in evs]
+    return total, store_ms, attn_ms, kern_ms, clocks
 
 
 def soak_clocks(step: DecodeStep, device, seconds=1.0):
@@ -302,6 +307,10 @@ def secondary(device, warmup: int, steps: int, peaks, which):
     hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops"]
     if "long" in which:
         res.update(_long_context(device, warmup, steps, hbm))
+    if "gqa" in which:
+        res.update(_split_sweep(workloads.gqa_decode_bf16(), "gqa_decode_bf16_split_sweep",
+                                "64 seqs ctx U[512,8192], Hq=32, Hkv=8, D=128, ps=16, bf16",
+                                (None, 1, 2, 3, 4, 8), device, warmup, steps, hbm))
     for name, maker in (("mixed_prefill_decode_bf16", workloads.mixed_prefill_decode_bf16),
                         ("mla_decode_bf16", workloads.mla_decode_bf16)):
         if name.split("_")[0] not in which:
@@ -331,28 +340,40 @@ def secondary(device, warmup: int, steps: int, peaks, which):
 
 def _long_context(device, warmup, steps, hbm):
     import workloads
+    return _split_sweep(workloads.long_context_decode_bf16(), "long_context_split_decode_bf16",
+                        "4 seqs ctx {32K,64K,96K,128K}, Hq=64, Hkv=8, D=128, ps=16, bf16",
+                        (None, 1, 4, 8, 16, 32, 64), device, warmup, steps, hbm)
+
+
+def _split_sweep(c3, name, desc, counts, device, warmup, steps, hbm):
     res = {}
-    c3 = workloads.long_context_decode_bf16()
     sweep = {}
-    for s in (None, 1, 4, 8, 16, 32, 64):
+    for s in counts:
         st = DecodeStep(c3, device, splits=s)
         for _ in range(warmup):
             st.attend()
         torch.cuda.synchronize(device)
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in kev:
+            a.record()
+            b.record()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(steps):
+        for i in range(steps):
+            st.pka.time_next_kernel(*kev[i])
             st.attend()
         e1.record()
         torch.cuda.synchronize(device)
         ms = e0.elapsed_time(e1) / steps
+        kms = statistics.mean(a.elapsed_time(b) for a, b in kev)
         sweep["heuristic" if s is None else str(s)] = {"splits": st.splits, "ms": ms,
-                                                        "kv_gbs": kv_bytes(c3) / ms / 1e6}
+                                                        "kv_gbs": kv_bytes(c3) / ms / 1e6, "kernel_ms": kms,
+                                                        "kernel_kv_gbs": kv_bytes(c3) / kms / 1e6}
         del st
     best = max(sweep.values(), key=lambda r: r["kv_gbs"])
     h = sweep["heuristic"]
-    res["long_context_split_decode_bf16"] = {
-        "config": "4 seqs ctx {32K,64K,96K,128K}, Hq=64, Hkv=8, D=128, ps=16, bf16",
+    res[name] = {
+        "config": desc,
         "kv_bytes": kv_bytes(c3), "heuristic_splits": h["splits"], "ms": h["ms"], "kv_gbs": h["kv_gbs"],
         "frac_hbm": h["kv_gbs"] / hbm, "best_splits": best["splits"], "best_kv_gbs": best["kv_gbs"],
         "sweep": sweep}
@@ -429,6 +450,30 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def profile_run(args):
+    """A few un-timed steps of one workload, for ncu captures of one kernel."""
+    import paged_kv_attention_20_gb300 as pka
+    import workloads
+    pka.build()
+    device = torch.device("cuda", 0)
+    n = args.profile_seqs
+    if args.profile == "gqa":
+        case = workloads.gqa_decode_bf16(num_seqs=n or 64)
+    elif args.profile == "long":
+        case = workloads.long_context_decode_bf16()
+    elif args.profile == "prefill":
+        case = workloads.mixed_prefill_decode_bf16(n_prefill=n or 8, n_decode=0 if n else 120)
+    else:
+        case = workloads.mla_decode_bf16(num_seqs=n or 128)
+    step = DecodeStep(case, device, splits=args.splits)
+    for _ in range(args.profile_iters):
+        step.store()
+        step.attend()
+    torch.cuda.synchronize(device)
+    print(json.dumps({"profile": args.profile, "queries": case.num_queries, "splits": step.splits,
+                      "kv_bytes": kv_bytes(case), "device_status": pka.device_status()}))
+
+
 # -------------------------------------------------------------------- main --
 
 def main():
@@ -438,13 +483,21 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--secondary", default="long,mixed,mla",
-                    help="comma list of secondary workloads: long, mixed, mla ('' for none)")
+                    help="comma list of secondary workloads: long, gqa, mixed, mla ('' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--splits", type=int, default=None, help="override the split heuristic")
+    ap.add_argument("--profile", choices=["gqa", "long", "prefill", "mla"], default=None,
+                    help="run a few un-timed steps of one workload (for ncu captures) and exit")
+    ap.add_argument("--profile-seqs", type=int, default=0,
+                    help="with --profile: number of sequences (0 = the full workload)")
+    ap.add_argument("--profile-iters", type=int, default=3)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = dist_info()
+    if args.profile:
+        profile_run(args)
+        return
 
     if args.impl == "reference":
         reference_arm(args, rank, world)
@@ -463,7 +516,7 @@ def main():
     case = workloads.gqa_decode_bf16()
     step = DecodeStep(case, device, splits=args.splits)
     sampler = ClockSampler(device.index or 0) if rank == 0 else None
-    total_ms, store_ms, attn_ms, clocks = time_step(step, args.steps, args.warmup, world, device, sampler)
+    total_ms, store_ms, attn_ms, kern_ms, clocks = time_step(step, args.steps, args.warmup, world, device, sampler)
     total_ms = max_over_ranks(total_ms, world, device)
     if rank == 0 and clocks is not None and clocks.get("samples", 0) < 3:
         clocks = soak_clocks(step, device)
@@ -472,7 +525,8 @@ def main():
     ms_per_step = total_ms / args.steps
     value = world * kvb * args.steps / (total_ms / 1e3) / 1e9
     attn_mean = statistics.mean(attn_ms)
-    achieved = kvb / (attn_mean / 1e3) / 1e9
+    kern_mean = statistics.mean(kern_ms)
+    achieved = kvb / (kern_mean / 1e3) / 1e9
     traffic = profile_traffic("decode_tma_gqa_decode_bf16",
                               ["paged_kv_attention_20_gb300/csrc/decode_tma.cu",
                                "paged_kv_attention_20_gb300/csrc/small_kernels.cu"])
@@ -492,10 +546,10 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "queries_per_s": world * case.num_queries * args.steps / (total_ms / 1e3),
         "frac_hbm_peak": value / world / peaks["hbm_gbs"],
-        "kernel_ms": {"store": statistics.mean(store_ms), "attention": attn_mean},
+        "kernel_ms": {"store": statistics.mean(store_ms), "attention_call": attn_mean, "decode_kernel": kern_mean},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "decode_tma_kernel<bf16,128,4> (+ merge_kernel when splits > 1)",
+                     "kernel": "decode_tma_kernel<bf16,128,4>, timed alone with CUDA events recorded by the library around its launch",
                      "peak_source": f"{peaks['source']} HBM copy bandwidth"},
         "clocks": clocks,
         "gpu_launches": args.steps * step.kernels_per_step(),

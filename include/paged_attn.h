@@ -265,6 +265,16 @@ pa_status paged_attn_forward_split_static(const pa_plan *plan, const void *q, co
                                           pa_stream_t stream);
 
 /*
+ * Profiling hook: the next attention call made on this thread records
+ * `start_event` on its stream just before launching its main kernel (the
+ * decode, MLA or prefill kernel -- the first one the call launches) and
+ * `stop_event` right after it.  Both are caller-created cudaEvent_t handles;
+ * the hook is consumed by that one call.  It changes no result; the benchmark
+ * uses it to time the dominant kernel alone.
+ */
+pa_status pa_time_next_kernel(void *start_event, void *stop_event);
+
+/*
  * Device-side status word.  Kernels that wait on hardware (mbarriers, tensor
  * memory) bound every wait; a wait that runs out sets this word to a non-zero
  * code (PA_DEVICE_TIMEOUT_*) and the kernel returns early, leaving the context

@@ -30,6 +30,7 @@ struct pa_plan {
 namespace {
 
 thread_local std::string g_error;
+thread_local cudaEvent_t g_time_start = nullptr, g_time_stop = nullptr;  // pa_time_next_kernel
 
 pa_status fail(pa_status st, const char *msg) {
     g_error = msg;
@@ -372,14 +373,24 @@ pa_status attention(const pa_plan *plan, const void *q, const void *k, const voi
     }
 
     cudaError_t e = cudaSuccess;
+    // optional profiling events around the call's main (first) kernel
+    cudaEvent_t t0 = g_time_start, t1 = g_time_stop;
+    g_time_start = g_time_stop = nullptr;
+    auto mark = [&](cudaEvent_t ev) {
+        if (ev && e == cudaSuccess) e = cudaEventRecord(ev, st);
+    };
     if (mla) {
         bool fast = pa::mla_supported(a);
+        mark(t0);
         e = fast ? pa::launch_mla(a, false, st) : pa::launch_decode(a, false, st);
+        mark(t1);
         if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, false, st);
     } else {
         bool tiles = plan->n_tiles > 0 && pa::prefill_supported(a);
         if (tiles) {
+            mark(t0);
             e = pa::launch_prefill(a, st);
+            mark(t1);
             if (e == cudaSuccess && plan->n_decode > 0) {
                 e = pa::launch_decode(a, true, st);
                 if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, true, st);
@@ -387,7 +398,9 @@ pa_status attention(const pa_plan *plan, const void *q, const void *k, const voi
         } else {
             // every query is a decode item: use the (longest-first) decode list
             const bool all_decode = plan->n_tiles == 0;
+            mark(t0);
             e = pa::launch_decode(a, all_decode, st);
+            mark(t1);
             if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, all_decode, st);
         }
     }
@@ -428,6 +441,12 @@ pa_status paged_mla_forward(const pa_plan *plan, const void *q, const void *qp, 
     return attention(plan, q, latent_cache, latent_cache, qp, pos_cache, out, num_heads, 1, latent_dim,
                      latent_dim, pos_dim, scale, causal, dtype, workspace, workspace_bytes, splits, true, true,
                      (cudaStream_t)stream, "paged_mla_forward");
+}
+
+pa_status pa_time_next_kernel(void *start_event, void *stop_event) {
+    g_time_start = static_cast<cudaEvent_t>(start_event);
+    g_time_stop = static_cast<cudaEvent_t>(stop_event);
+    return PA_OK;
 }
 
 pa_status pa_device_status(int32_t *code, int32_t clear) {

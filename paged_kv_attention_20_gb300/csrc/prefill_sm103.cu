@@ -52,14 +52,14 @@ struct Smem {
     uint8_t q[kTileBytes];
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kTileBytes];
-    uint8_t p[kTileBytes];
+    uint8_t p[2][kTileBytes];      // P double buffer (tile kt uses p[kt & 1])
     uint64_t q_full;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t s_full[2];
     uint64_t s_free[2];
     uint64_t p_ready;
-    uint64_t o_done;
+    uint64_t o_done[2];            // P.V of tile kt done -> o_done[kt & 1]
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -123,7 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&s.s_free[i], kM);
         }
         mbar_init(&s.p_ready, kM);
-        mbar_init(&s.o_done, 1);
+        mbar_init(&s.o_done[0], 1);
+        mbar_init(&s.o_done[1], 1);
         s.abort = 0;
         fence_mbar_init();
     }
@@ -158,9 +159,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (s.abort) break;
                 mbar_arrive_expect_tx(&s.kv_full[st], 2 * kTileBytes);
                 const int pages_per_tile = kN / ps;
-                for (int i = 0; i < pages_per_tile; ++i) {
+                int rows[8];               // <= 8 pages per tile (page_size >= 16); loads issued together
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
                     const int lp = kt * pages_per_tile + i;
-                    const int row = lp < used_pages ? trow[lp] * ps : oob_row;
+                    rows[i] = (i < pages_per_tile && lp < used_pages) ? trow[lp] * ps : oob_row;
+                }
+                for (int i = 0; i < pages_per_tile; ++i) {
+                    const int row = rows[i];
                     const uint32_t off = (uint32_t)i * ps * 128;
                     tma_load_3d(s.k[st] + off, &tm_k, 0, kvh, row, &s.kv_full[st]);
                     tma_load_3d(s.k[st] + kHalfBytes + off, &tm_k, 64, kvh, row, &s.kv_full[st]);
@@ -174,20 +180,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc_s = idesc_f16(kM, kN, prm.bf16 != 0, false, false);
             const uint32_t idesc_o = idesc_f16(kM, kD, prm.bf16 != 0, false, true);
-            const uint32_t q_addr = smem_u32(s.q), p_addr = smem_u32(s.p);
+            const uint32_t q_addr = smem_u32(s.q);
             bool ok = mbar_wait(&s.q_full, 0);
             auto issue_pv = [&](int kt) -> bool {
                 if (!mbar_wait(&s.p_ready, kt & 1)) return false;
                 tc_fence_after();
                 const int st = kt % kStages;
                 const uint32_t v_addr = smem_u32(s.v[st]);
+                const uint32_t p_addr = smem_u32(s.p[kt & 1]);
                 for (int ks = 0; ks < kN / 16; ++ks) {
                     const uint64_t a = smem_desc(p_addr + (ks / 4) * kHalfBytes + (ks % 4) * 32, 16, 1024,
                                                  kLayoutSwizzle128B);
                     const uint64_t b = smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, kLayoutSwizzle128B);
                     mma_f16_ss(tmem_o, a, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
                 }
-                mma_commit(&s.o_done);
+                mma_commit(&s.o_done[kt & 1]);
                 mma_commit(&s.kv_empty[st]);
                 return true;
             };
@@ -222,28 +229,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const int kbase = kt * kN;
-            // pass 1: tile max over visible keys
-            float mt = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < kN; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem_s[sb] + lane_off + c, v);
-                tmem_wait_ld();
+            // one pass: the row's 128 scores into registers (four loads, one wait)
+            uint32_t sv[kN];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (kbase + c + i < vis_end) mt = fmaxf(mt, __uint_as_float(v[i]) * prm.scale_log2);
+            for (int c = 0; c < kN; c += 32) tmem_ld32(tmem_s[sb] + lane_off + c, sv + c);
+            tmem_wait_ld();
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kN; ++c) {
+                const float x = kbase + c < vis_end ? __uint_as_float(sv[c]) * prm.scale_log2 : -INFINITY;
+                sv[c] = __float_as_uint(x);
+                mt = fmaxf(mt, x);
             }
+            tc_fence_before();
+            mbar_arrive(&s.s_free[sb]);            // S buffer may be overwritten now
             float alpha = 1.f;
             if (mt > m_ref + kSlack) {
                 alpha = exp2f(m_ref - mt);
                 m_ref = mt;
             }
-            // the previous P.V must be done before P is overwritten or O rescaled
-            if (kt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done, (kt - 1) & 1));
-            if (!ok) break;
-            tc_fence_after();
-            // tcgen05.ld/st are warp-collective: the whole warp rescales when any row needs it
+            // P buffer kt&1 was last read by the P.V of tile kt-2
+            if (kt >= 2) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[kt & 1], ((kt / 2) - 1) & 1));
+                if (!ok) break;
+            }
+            // rescaling O needs the previous P.V finished (rare: the row max moved by > 2^8)
             if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(kt - 1) & 1], ((kt - 1) / 2) & 1));
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < kD; c += 16) {
                     uint32_t v[16];
@@ -255,18 +269,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
             }
-            // pass 2: P = exp2(s - m_ref) as 16-bit, written in the swizzled K-major layout
+            // P = exp2(s - m_ref) as 16-bit, written in the swizzled K-major layout
             float lsum = 0.f;
-#pragma unroll 1
+            uint8_t *pbuf = s.p[kt & 1];
+#pragma unroll
             for (int c = 0; c < kN; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem_s[sb] + lane_off + c, v);
-                tmem_wait_ld();
                 float p[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const bool vis = kbase + c + i < vis_end;
-                    p[i] = vis ? exp2f(__uint_as_float(v[i]) * prm.scale_log2 - m_ref) : 0.f;
+                    p[i] = exp2f(__uint_as_float(sv[c + i]) - m_ref);
                     lsum += p[i];
                 }
                 uint4 w0, w1;
@@ -275,12 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 w1.x = pack2<T>(p[8], p[9]);   w1.y = pack2<T>(p[10], p[11]);
                 w1.z = pack2<T>(p[12], p[13]); w1.w = pack2<T>(p[14], p[15]);
                 const int half = c / 64, chunk = (c % 64) / 8;  // two 16-byte chunks per 16 keys
-                uint8_t *row = s.p + half * kHalfBytes + r * 128;
+                uint8_t *row = pbuf + half * kHalfBytes + r * 128;
                 *reinterpret_cast<uint4 *>(row + (((chunk) ^ (r & 7)) * 16)) = w0;
                 *reinterpret_cast<uint4 *>(row + (((chunk + 1) ^ (r & 7)) * 16)) = w1;
             }
-            tc_fence_before();
-            mbar_arrive(&s.s_free[sb]);
             l = l * alpha + lsum;
             // V rows at or past the sequence end (tail slots) must not reach the MMA
             if (kbase + kN > seq_len) {
@@ -297,9 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             fence_proxy_async_smem();
+            tc_fence_before();
             mbar_arrive(&s.p_ready);
         }
-        if (ok && n_kt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done, (n_kt - 1) & 1));
+        if (ok && n_kt > 0)
+            ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) & 1], ((n_kt - 1) / 2) & 1));
         if (!ok) {
             set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_SOFTMAX);
         } else {
