@@ -259,24 +259,29 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
         }
         __syncwarp();
 
-        // online softmax, two heads per pass (one per half-warp)
+        // online softmax, two heads per pass (one per half-warp).  Weights use
+        // the current reference max; only when some score exceeds it by more
+        // than 2^8 (the first tile, then rarely) does the half-warp reduce its
+        // tile max and move the reference.  Weight sums stay per lane until the end.
         const int t16 = lane & 15;
 #pragma unroll
         for (int k = 0; k < HP; ++k) {
             const int g = 2 * k + (lane >> 4);
             const bool gv = g < GH;
             const float s = (gv && t16 < valid) ? sp[2 * C::TT * GH + t16 * GH + g] : -INFINITY;
-            float mt = s;
+            float alpha = 1.f;
+            if (__any_sync(0xffffffffu, s > m_ref[k] + kSlack)) {
+                float mt = s;
 #pragma unroll
-            for (int o = 8; o; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-            const float nref = (mt > m_ref[k] + kSlack) ? mt : m_ref[k];
-            const float alpha = exp2f(m_ref[k] - nref);
-            const float p = exp2f(s - nref);
-            float psum = p;
-#pragma unroll
-            for (int o = 8; o; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
-            l_run[k] = l_run[k] * alpha + psum;
-            m_ref[k] = nref;
+                for (int o = 8; o; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+                if (mt > m_ref[k] + kSlack) {
+                    alpha = exp2f(m_ref[k] - mt);
+                    m_ref[k] = mt;
+                    l_run[k] *= alpha;
+                }
+            }
+            const float p = exp2f(s - m_ref[k]);
+            l_run[k] += p;
             if (gv) {
                 reinterpret_cast<float2 *>(sp)[t16 * GH + g] = make_float2(p, p);
                 if (t16 == 0) al[g] = alpha;
@@ -341,10 +346,13 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
             reinterpret_cast<float2 *>(mo + ((size_t)warp * GH + g) * D + lane * C::CPL)[c] = acc[g][c];
 #pragma unroll
     for (int k = 0; k < HP; ++k) {
+        float lk = l_run[k];
+#pragma unroll
+        for (int o = 8; o; o >>= 1) lk += __shfl_xor_sync(0xffffffffu, lk, o);
         const int g = 2 * k + (lane >> 4);
         if (g < GH && (lane & 15) == 0) {
             ml[(warp * GH + g) * 2] = m_ref[k];
-            ml[(warp * GH + g) * 2 + 1] = l_run[k];
+            ml[(warp * GH + g) * 2 + 1] = lk;
         }
     }
     __syncthreads();

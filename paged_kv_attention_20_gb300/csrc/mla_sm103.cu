@@ -20,6 +20,8 @@
 //
 // Roles per CTA: warps 0-3 exchange/softmax/epilogue (thread r = head r, TMEM
 // lane r), warp 4 TMA producer (64-key tiles, 2 stages), warp 5 MMA issuer.
+// P (16-bit) is written back over its row of the S buffer in TMEM and read
+// from there by the P.V MMA, so the two S buffers double as P buffers.
 // Key tiles are one page at page_size 64 (several boxes for smaller pages).
 // Keys at or past the sequence end are masked and their latent rows zeroed
 // before P.V.  All waits are bounded (timeout -> device status word).
@@ -53,15 +55,13 @@ constexpr float kSlack = 8.f;
 struct Smem {
     uint8_t q[5][kBlk];                  // own Q blocks (rank 0: q[0:256] + qp; rank 1: q[256:512])
     uint8_t kv[kStages][5][kKBlk];       // own latent blocks 0..3 (+ position block 4 on rank 0)
-    uint8_t p[kBlk];                     // P, 128 x 64 16-bit, swizzled K-major
     float recv[kHeads * kRecvStride];    // peer's partial scores
     uint64_t q_full;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t s_full[2];
-    uint64_t s_free[2];
     uint64_t p_ready;
-    uint64_t o_done;
+    uint64_t o_done[2];                  // P.V of tile kt done -> o_done[kt & 1]
     uint64_t recv_full;                  // local expect_tx + the peer's asynchronous stores (bytes)
     uint64_t can_send;                   // arrived by the peer's 4 row warps after reading its recv
     uint32_t tmem_base;
@@ -188,10 +188,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.s_full[i], 1);
-            mbar_init(&s.s_free[i], kHeads);
+            mbar_init(&s.o_done[i], 1);
         }
         mbar_init(&s.p_ready, kHeads);
-        mbar_init(&s.o_done, 1);
         mbar_init(&s.recv_full, 1);
         mbar_init(&s.can_send, 4);
         s.abort = 0;
@@ -249,20 +248,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&s.p_ready, kt & 1)) return false;
                 tc_fence_after();
                 const int st = kt % kStages;
-                const uint32_t v_addr = smem_u32(s.kv[st][0]), p_addr = smem_u32(s.p);
+                const uint32_t v_addr = smem_u32(s.kv[st][0]);
+                const uint32_t p_tmem = tmem_s[kt & 1];           // P (16-bit pairs) over the S columns
                 for (int ks = 0; ks < kN / 16; ++ks) {
-                    const uint64_t a = smem_desc(p_addr + ks * 32, 16, 1024, kLayoutSwizzle128B);
                     const uint64_t b = smem_desc(v_addr + ks * 2048, kKBlk, 1024, kLayoutSwizzle128B);
-                    mma_f16_ss(tmem_o, a, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
+                    mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
                 }
-                mma_commit(&s.o_done);
+                mma_commit(&s.o_done[kt & 1]);
                 mma_commit(&s.kv_empty[st]);
                 return true;
             };
             for (int kt = 0; ok && kt < n_kt; ++kt) {
                 const int st = kt % kStages, sb = kt & 1;
                 if (!mbar_wait(&s.kv_full[st], (kt / kStages) & 1)) { ok = false; break; }
-                if (kt >= 2 && !mbar_wait(&s.s_free[sb], ((kt / 2) - 1) & 1)) { ok = false; break; }
+                // the buffer's previous tile (kt-2) must be through its P.V (P lives in it)
+                if (kt >= 2 && !mbar_wait(&s.o_done[sb], ((kt / 2) - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 for (int blk = 0; blk < nkb; ++blk)
                     for (int k = 0; k < 4; ++k) {
@@ -304,8 +304,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) sc[c + i] = __uint_as_float(v[i]);
             }
-            tc_fence_before();
-            mbar_arrive(&s.s_free[sb]);
             // this tile's receive: 128 rows x 64 floats from the peer
             if (r == 0) mbar_arrive_expect_tx(&s.recv_full, kHeads * kN * 4);
             // send my partial to the peer (its buffer is free once it read the previous one)
@@ -338,12 +336,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 alpha = exp2f(m_ref - mt);
                 m_ref = mt;
             }
-            if (kt > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done, (kt - 1) & 1));
-                if (!ok) break;
-            }
-            tc_fence_after();
+            // rescaling O needs the previous P.V finished (rare: the row max moved by > 2^8)
             if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(kt - 1) & 1], ((kt - 1) / 2) & 1));
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < 256; c += 16) {
                     uint32_t v[16];
@@ -355,20 +352,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
             }
+            // P = exp2(s - m_ref) as 16-bit pairs over this row's S columns (already read)
             float lsum = 0.f;
 #pragma unroll
-            for (int c = 0; c < kN; c += 8) {
-                float p[8];
+            for (int c = 0; c < kN; c += 32) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    p[i] = exp2f(sc[c + i] - m_ref);
-                    lsum += p[i];
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = exp2f(sc[c + 2 * i] - m_ref);
+                    const float p1 = exp2f(sc[c + 2 * i + 1] - m_ref);
+                    lsum += p0 + p1;
+                    pk[i] = pack2<T>(p0, p1);
                 }
-                uint4 w;
-                w.x = pack2<T>(p[0], p[1]); w.y = pack2<T>(p[2], p[3]);
-                w.z = pack2<T>(p[4], p[5]); w.w = pack2<T>(p[6], p[7]);
-                *reinterpret_cast<uint4 *>(s.p + r * 128 + (((c / 8) ^ (r & 7)) * 16)) = w;
+                tmem_st16(tmem_s[sb] + lane_off + c / 2, pk);
             }
+            tmem_wait_st();
             l = l * alpha + lsum;
             // latent rows past the visible range must not reach P.V (tail slots may hold NaN)
             if (valid < kN) {
@@ -387,7 +385,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&s.p_ready);
         }
-        if (ok && n_kt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done, (n_kt - 1) & 1));
+        if (ok && n_kt > 0)
+            ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) & 1], ((n_kt - 1) / 2) & 1));
         if (!ok) {
             atomicExch(&s.abort, 1);
             atomicCAS(prm.status, 0, PA_DEVICE_TIMEOUT_SOFTMAX);

@@ -11,10 +11,11 @@
 //              (TMEM lane r);
 //   warp 4     TMA producer: Q once, then K/V tiles of 128 keys gathered
 //              page by page through the block table (one 16-row box per
-//              page and 64-column half, 128-byte swizzle), 2-stage ring;
-//   warp 5     MMA issuer: S = Q K^T into one of two TMEM S buffers, then
-//              O += P V with P (bf16, written by the softmax warps in the
-//              swizzled K-major layout) in shared memory.
+//              page and 64-column half, 128-byte swizzle);
+//   warp 5     MMA issuer: S = Q K^T into one of two TMEM buffers, then
+//              O += P V with P read from tensor memory: the softmax warps
+//              overwrite their row of the S buffer with P as 16-bit pairs.
+// K/V tiles use a 3-stage shared-memory ring; P never touches shared memory.
 // Key tiles past the last query's position are never loaded; the diagonal
 // tiles are masked per row.  Keys at or past the sequence length never reach
 // P.V: their scores are masked and their V rows are zeroed in shared memory
@@ -40,7 +41,7 @@ using namespace tc;
 constexpr int kM = 128;          // queries per tile (TMEM lanes)
 constexpr int kN = 128;          // keys per tile
 constexpr int kD = 128;          // head dim (== value dim)
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kThreads = 192;
 constexpr uint32_t kHalfBytes = kM * 128;          // one 64-column half of a 128-row tile
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;    // 32 KB
@@ -52,12 +53,10 @@ struct Smem {
     uint8_t q[kTileBytes];
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kTileBytes];
-    uint8_t p[2][kTileBytes];      // P double buffer (tile kt uses p[kt & 1])
     uint64_t q_full;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t s_full[2];
-    uint64_t s_free[2];
     uint64_t p_ready;
     uint64_t o_done[2];            // P.V of tile kt done -> o_done[kt & 1]
     uint32_t tmem_base;
@@ -118,10 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&s.kv_full[i], 1);
             mbar_init(&s.kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s.s_full[i], 1);
-            mbar_init(&s.s_free[i], kM);
-        }
+        for (int i = 0; i < 2; ++i) mbar_init(&s.s_full[i], 1);
         mbar_init(&s.p_ready, kM);
         mbar_init(&s.o_done[0], 1);
         mbar_init(&s.o_done[1], 1);
@@ -187,12 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int st = kt % kStages;
                 const uint32_t v_addr = smem_u32(s.v[st]);
-                const uint32_t p_addr = smem_u32(s.p[kt & 1]);
+                const uint32_t p_tmem = tmem_s[kt & 1];          // P (16-bit pairs) over the S columns
                 for (int ks = 0; ks < kN / 16; ++ks) {
-                    const uint64_t a = smem_desc(p_addr + (ks / 4) * kHalfBytes + (ks % 4) * 32, 16, 1024,
-                                                 kLayoutSwizzle128B);
                     const uint64_t b = smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, kLayoutSwizzle128B);
-                    mma_f16_ss(tmem_o, a, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
+                    mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
                 }
                 mma_commit(&s.o_done[kt & 1]);
                 mma_commit(&s.kv_empty[st]);
@@ -201,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kt = 0; ok && kt < n_kt; ++kt) {
                 const int st = kt % kStages, sb = kt & 1;
                 if (!mbar_wait(&s.kv_full[st], (kt / kStages) & 1)) { ok = false; break; }
-                if (kt >= 2 && !mbar_wait(&s.s_free[sb], ((kt / 2) - 1) & 1)) { ok = false; break; }
+                // the buffer's previous tile (kt-2) must be through its P.V (P lives in it)
+                if (kt >= 2 && !mbar_wait(&s.o_done[sb], ((kt / 2) - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t k_addr = smem_u32(s.k[st]);
                 for (int ks = 0; ks < kD / 16; ++ks) {
@@ -229,29 +224,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const int kbase = kt * kN;
-            // one pass: the row's 128 scores into registers (four loads, one wait)
+            // the row's 128 scores into registers (four loads, one wait)
             uint32_t sv[kN];
 #pragma unroll
             for (int c = 0; c < kN; c += 32) tmem_ld32(tmem_s[sb] + lane_off + c, sv + c);
             tmem_wait_ld();
             float mt = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kN; ++c) {
-                const float x = kbase + c < vis_end ? __uint_as_float(sv[c]) * prm.scale_log2 : -INFINITY;
-                sv[c] = __float_as_uint(x);
-                mt = fmaxf(mt, x);
-            }
-            tc_fence_before();
-            mbar_arrive(&s.s_free[sb]);            // S buffer may be overwritten now
+            for (int c = 0; c < kN; ++c)
+                if (kbase + c < vis_end) mt = fmaxf(mt, __uint_as_float(sv[c]) * prm.scale_log2);
             float alpha = 1.f;
             if (mt > m_ref + kSlack) {
                 alpha = exp2f(m_ref - mt);
                 m_ref = mt;
-            }
-            // P buffer kt&1 was last read by the P.V of tile kt-2
-            if (kt >= 2) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[kt & 1], ((kt / 2) - 1) & 1));
-                if (!ok) break;
             }
             // rescaling O needs the previous P.V finished (rare: the row max moved by > 2^8)
             if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -269,27 +254,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
             }
-            // P = exp2(s - m_ref) as 16-bit, written in the swizzled K-major layout
+            // P = exp2(s - m_ref) as 16-bit pairs, written over this row's S columns
+            // (each 32-score chunk is re-read from TMEM before its P overwrites it)
             float lsum = 0.f;
-            uint8_t *pbuf = s.p[kt & 1];
-#pragma unroll
-            for (int c = 0; c < kN; c += 16) {
-                float p[16];
+#pragma unroll 1
+            for (int c = 0; c < kN; c += 32) {
+                uint32_t sc[32], pk[16];
+                tmem_ld32(tmem_s[sb] + lane_off + c, sc);
+                tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    p[i] = exp2f(__uint_as_float(sv[c + i]) - m_ref);
-                    lsum += p[i];
+                    const int k0 = kbase + c + 2 * i;
+                    const float p0 = k0 < vis_end ? exp2f(__uint_as_float(sc[2 * i]) * prm.scale_log2 - m_ref) : 0.f;
+                    const float p1 = k0 + 1 < vis_end ? exp2f(__uint_as_float(sc[2 * i + 1]) * prm.scale_log2 - m_ref) : 0.f;
+                    lsum += p0 + p1;
+                    pk[i] = pack2<T>(p0, p1);
                 }
-                uint4 w0, w1;
-                w0.x = pack2<T>(p[0], p[1]);   w0.y = pack2<T>(p[2], p[3]);
-                w0.z = pack2<T>(p[4], p[5]);   w0.w = pack2<T>(p[6], p[7]);
-                w1.x = pack2<T>(p[8], p[9]);   w1.y = pack2<T>(p[10], p[11]);
-                w1.z = pack2<T>(p[12], p[13]); w1.w = pack2<T>(p[14], p[15]);
-                const int half = c / 64, chunk = (c % 64) / 8;  // two 16-byte chunks per 16 keys
-                uint8_t *row = pbuf + half * kHalfBytes + r * 128;
-                *reinterpret_cast<uint4 *>(row + (((chunk) ^ (r & 7)) * 16)) = w0;
-                *reinterpret_cast<uint4 *>(row + (((chunk + 1) ^ (r & 7)) * 16)) = w1;
+                tmem_st16(tmem_s[sb] + lane_off + c / 2, pk);
             }
+            tmem_wait_st();
             l = l * alpha + lsum;
             // V rows at or past the sequence end (tail slots) must not reach the MMA
             if (kbase + kN > seq_len) {
@@ -305,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            fence_proxy_async_smem();
+            fence_proxy_async_smem();      // zeroed V rows (if any) before the tensor core reads them
             tc_fence_before();
             mbar_arrive(&s.p_ready);
         }
