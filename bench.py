@@ -165,12 +165,20 @@ def dist_info():
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
+    """Largest value over the ranks (device: where the collective's tensor lives)."""
     if world == 1:
         return x
     import torch.distributed as dist
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_step: float, steps: int, local_ms: float, world: int, device) -> tuple:
+    """Weak scaling over independent replicas: every rank processes `units_per_step`
+    per step; the job time is the slowest rank's.  Returns (units per second, max ms)."""
+    total_ms = max_over_ranks(local_ms, world, device)
+    return world * units_per_step * steps / (total_ms / 1e3), total_ms
 
 
 def barrier(world: int):
@@ -516,14 +524,14 @@ def main():
     case = workloads.gqa_decode_bf16()
     step = DecodeStep(case, device, splits=args.splits)
     sampler = ClockSampler(device.index or 0) if rank == 0 else None
-    total_ms, store_ms, attn_ms, kern_ms, clocks = time_step(step, args.steps, args.warmup, world, device, sampler)
-    total_ms = max_over_ranks(total_ms, world, device)
+    local_ms, store_ms, attn_ms, kern_ms, clocks = time_step(step, args.steps, args.warmup, world, device, sampler)
+    kvb = kv_bytes(case)
+    rate, total_ms = whole_job_rate(kvb, args.steps, local_ms, world, device)
     if rank == 0 and clocks is not None and clocks.get("samples", 0) < 3:
         clocks = soak_clocks(step, device)
 
-    kvb = kv_bytes(case)
     ms_per_step = total_ms / args.steps
-    value = world * kvb * args.steps / (total_ms / 1e3) / 1e9
+    value = rate / 1e9
     attn_mean = statistics.mean(attn_ms)
     kern_mean = statistics.mean(kern_ms)
     achieved = kvb / (kern_mean / 1e3) / 1e9

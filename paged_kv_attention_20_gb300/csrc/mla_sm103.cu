@@ -47,7 +47,6 @@ constexpr int kStages = 2;
 constexpr int kThreads = 192;
 constexpr int kBlk = kHeads * 128;        // one 64-column block of the Q tile (bytes)
 constexpr int kKBlk = kN * 128;           // one 64-column block of a key tile (bytes)
-constexpr int kRecvStride = kN + 4;       // padded row of the peer's partial scores (floats)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kSlack = 8.f;
@@ -55,15 +54,15 @@ constexpr float kSlack = 8.f;
 struct Smem {
     uint8_t q[5][kBlk];                  // own Q blocks (rank 0: q[0:256] + qp; rank 1: q[256:512])
     uint8_t kv[kStages][5][kKBlk];       // own latent blocks 0..3 (+ position block 4 on rank 0)
-    float recv[kHeads * kRecvStride];    // peer's partial scores
+    float recv[2][kHeads * kN];          // peer's partial scores, double buffered, 16-byte chunks XOR-swizzled
     uint64_t q_full;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t s_full[2];
     uint64_t p_ready;
     uint64_t o_done[2];                  // P.V of tile kt done -> o_done[kt & 1]
-    uint64_t recv_full;                  // local expect_tx + the peer's asynchronous stores (bytes)
-    uint64_t can_send;                   // arrived by the peer's 4 row warps after reading its recv
+    uint64_t recv_full[2];               // local expect_tx + the peer's asynchronous stores (bytes)
+    uint64_t can_send[2];                // arrived by the peer's 4 row warps after reading its recv[b]
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -191,8 +190,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(&s.o_done[i], 1);
         }
         mbar_init(&s.p_ready, kHeads);
-        mbar_init(&s.recv_full, 1);
-        mbar_init(&s.can_send, 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.recv_full[i], 1);
+            mbar_init(&s.can_send[i], 4);
+        }
         s.abort = 0;
         fence_mbar_init();
     }
@@ -281,55 +282,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------- exchange / softmax / epilogue rows --
+        // Software pipeline: the partial scores of tile kt+1 are read from TMEM
+        // and sent to the peer before tile kt is combined, so the cross-SM
+        // exchange latency overlaps the previous tile's softmax.
         const int r = tid;
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        const uint32_t recv_peer = peer_addr(smem_u32(&s.recv[r * kRecvStride]), peer);
-        const uint32_t recv_full_peer = peer_addr(smem_u32(&s.recv_full), peer);
-        const uint32_t can_send_peer = peer_addr(smem_u32(&s.can_send), peer);
+        uint32_t recv_peer[2], recv_full_peer[2], can_send_peer[2];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            recv_peer[b] = peer_addr(smem_u32(&s.recv[b][r * kN]), peer);
+            recv_full_peer[b] = peer_addr(smem_u32(&s.recv_full[b]), peer);
+            can_send_peer[b] = peer_addr(smem_u32(&s.can_send[b]), peer);
+        }
+        const int sw = r & 15;                   // chunk swizzle of row r
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int kt = 0; kt < n_kt; ++kt) {
-            const int sb = kt & 1;
-            const int64_t kbase = j0 + (int64_t)kt * kN;
-            const int valid = (int)((j1 - kbase) < kN ? (j1 - kbase) : kN);
-            ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[sb], (kt / 2) & 1));
-            if (!ok) break;
+        float cur[kN], nxt[kN];
+        // read partial scores of tile t from TMEM and send them to the peer's recv[t & 1]
+        auto fetch_and_send = [&](int t, float (&sc)[kN]) -> bool {
+            const int b = t & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.s_full[b], (t / 2) & 1))) return false;
             tc_fence_after();
-            float sc[kN];
 #pragma unroll
             for (int c = 0; c < kN; c += 16) {
                 uint32_t v[16];
-                tmem_ld16(tmem_s[sb] + lane_off + c, v);
+                tmem_ld16(tmem_s[b] + lane_off + c, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) sc[c + i] = __uint_as_float(v[i]);
             }
-            // this tile's receive: 128 rows x 64 floats from the peer
-            if (r == 0) mbar_arrive_expect_tx(&s.recv_full, kHeads * kN * 4);
-            // send my partial to the peer (its buffer is free once it read the previous one)
-            if (kt > 0) {
-                ok = __all_sync(0xffffffffu, wait_cluster(&s.can_send, (kt - 1) & 1));
+            if (r == 0) mbar_arrive_expect_tx(&s.recv_full[b], kHeads * kN * 4);   // my receive of tile t
+            if (t >= 2 && !__all_sync(0xffffffffu, wait_cluster(&s.can_send[b], ((t / 2) - 1) & 1))) return false;
+#pragma unroll
+            for (int c = 0; c < kN / 4; ++c)
+                st_async_v4(recv_peer[b] + ((c ^ sw) * 16), sc[4 * c], sc[4 * c + 1], sc[4 * c + 2], sc[4 * c + 3],
+                            recv_full_peer[b]);
+            return true;
+        };
+        if (n_kt > 0) ok = fetch_and_send(0, cur);
+        for (int kt = 0; ok && kt < n_kt; ++kt) {
+            const int sb = kt & 1;
+            const int64_t kbase = j0 + (int64_t)kt * kN;
+            const int valid = (int)((j1 - kbase) < kN ? (j1 - kbase) : kN);
+            if (kt + 1 < n_kt) {
+                ok = fetch_and_send(kt + 1, nxt);
                 if (!ok) break;
             }
-#pragma unroll
-            for (int c = 0; c < kN; c += 4)
-                st_async_v4(recv_peer + c * 4, sc[c], sc[c + 1], sc[c + 2], sc[c + 3], recv_full_peer);
-            ok = __all_sync(0xffffffffu, wait_cluster(&s.recv_full, kt & 1));
+            ok = __all_sync(0xffffffffu, wait_cluster(&s.recv_full[sb], (kt / 2) & 1));
             if (!ok) break;
-            const float *mine = &s.recv[r * kRecvStride];
+            const float *mine = &s.recv[sb][r * kN];
 #pragma unroll
-            for (int c = 0; c < kN; c += 4) {
-                const float4 o = *reinterpret_cast<const float4 *>(mine + c);
-                sc[c] += o.x; sc[c + 1] += o.y; sc[c + 2] += o.z; sc[c + 3] += o.w;
+            for (int c = 0; c < kN / 4; ++c) {
+                const float4 o = *reinterpret_cast<const float4 *>(mine + ((c ^ sw) * 4));
+                cur[4 * c] += o.x; cur[4 * c + 1] += o.y; cur[4 * c + 2] += o.z; cur[4 * c + 3] += o.w;
             }
             __syncwarp();
-            if (lane == 0) arrive_remote(can_send_peer);   // this warp's rows are read
+            if (lane == 0) arrive_remote(can_send_peer[sb]);   // this warp's rows of recv[sb] are read
             // online softmax (identical on both CTAs)
             float mt = -INFINITY;
 #pragma unroll
             for (int c = 0; c < kN; ++c) {
-                sc[c] = c < valid ? sc[c] * prm.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, sc[c]);
+                cur[c] = c < valid ? cur[c] * prm.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, cur[c]);
             }
             float alpha = 1.f;
             if (mt > m_ref + kSlack) {
@@ -359,8 +373,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = exp2f(sc[c + 2 * i] - m_ref);
-                    const float p1 = exp2f(sc[c + 2 * i + 1] - m_ref);
+                    const float p0 = exp2f(cur[c + 2 * i] - m_ref);
+                    const float p1 = exp2f(cur[c + 2 * i + 1] - m_ref);
                     lsum += p0 + p1;
                     pk[i] = pack2<T>(p0, p1);
                 }
@@ -384,6 +398,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&s.p_ready);
+#pragma unroll
+            for (int c = 0; c < kN; ++c) cur[c] = nxt[c];
         }
         if (ok && n_kt > 0)
             ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) & 1], ((n_kt - 1) / 2) & 1));

@@ -137,6 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 4) {
         // ---------------------------------------------------- TMA producer --
+        // Lane 0 owns the barriers; lanes 0..pages_per_tile-1 each gather one
+        // page of K and V (4 boxes), so the box issue runs 8 lanes wide.
+        const int pages_per_tile = kN / ps;
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -144,31 +147,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&s.q_full, kTileBytes);
             tma_load_3d(s.q, &tm_q, 0, h, q0, &s.q_full);
             tma_load_3d(s.q + kHalfBytes, &tm_q, 64, h, q0, &s.q_full);
-            const int oob_row = prm.plan.pages * ps;          // rows >= this read as zeros
-            const int used_pages = (seq_len + ps - 1) / ps;
-            for (int kt = 0; kt < n_kt; ++kt) {
-                const int st = kt % kStages;
+        }
+        const int oob_row = prm.plan.pages * ps;          // rows >= this read as zeros
+        const int used_pages = (seq_len + ps - 1) / ps;
+        for (int kt = 0; kt < n_kt; ++kt) {
+            const int st = kt % kStages;
+            bool go = true;
+            if (lane == 0) {
                 if (kt >= kStages && !mbar_wait(&s.kv_empty[st], ((kt / kStages) - 1) & 1)) {
                     set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
-                    break;
+                    go = false;
+                } else {
+                    mbar_arrive_expect_tx(&s.kv_full[st], 2 * kTileBytes);
                 }
-                if (s.abort) break;
-                mbar_arrive_expect_tx(&s.kv_full[st], 2 * kTileBytes);
-                const int pages_per_tile = kN / ps;
-                int rows[8];               // <= 8 pages per tile (page_size >= 16); loads issued together
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int lp = kt * pages_per_tile + i;
-                    rows[i] = (i < pages_per_tile && lp < used_pages) ? trow[lp] * ps : oob_row;
-                }
-                for (int i = 0; i < pages_per_tile; ++i) {
-                    const int row = rows[i];
-                    const uint32_t off = (uint32_t)i * ps * 128;
-                    tma_load_3d(s.k[st] + off, &tm_k, 0, kvh, row, &s.kv_full[st]);
-                    tma_load_3d(s.k[st] + kHalfBytes + off, &tm_k, 64, kvh, row, &s.kv_full[st]);
-                    tma_load_3d(s.v[st] + off, &tm_v, 0, kvh, row, &s.kv_full[st]);
-                    tma_load_3d(s.v[st] + kHalfBytes + off, &tm_v, 64, kvh, row, &s.kv_full[st]);
-                }
+            }
+            go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+            if (!go) break;
+            if (lane < pages_per_tile) {
+                const int lp = kt * pages_per_tile + lane;
+                const int row = lp < used_pages ? trow[lp] * ps : oob_row;
+                const uint32_t off = (uint32_t)lane * ps * 128;
+                tma_load_3d(s.k[st] + off, &tm_k, 0, kvh, row, &s.kv_full[st]);
+                tma_load_3d(s.k[st] + kHalfBytes + off, &tm_k, 64, kvh, row, &s.kv_full[st]);
+                tma_load_3d(s.v[st] + off, &tm_v, 0, kvh, row, &s.kv_full[st]);
+                tma_load_3d(s.v[st] + kHalfBytes + off, &tm_v, 64, kvh, row, &s.kv_full[st]);
             }
         }
     } else if (warp == 5) {
