@@ -21,7 +21,8 @@
 // Roles per CTA: warps 0-3 exchange/softmax/epilogue (thread r = head r, TMEM
 // lane r), warp 4 TMA producer (64-key tiles, 2 stages), warp 5 MMA issuer.
 // P (16-bit) is written back over its row of the S buffer in TMEM and read
-// from there by the P.V MMA, so the two S buffers double as P buffers.
+// from there by the P.V MMA; three S/P buffers let S of the next tile be
+// computed while the current tile's P waits for its P.V.
 // Key tiles are one page at page_size 64 (several boxes for smaller pages).
 // Keys at or past the sequence end are masked and their latent rows zeroed
 // before P.V.  All waits are bounded (timeout -> device status word).
@@ -58,9 +59,9 @@ struct Smem {
     uint64_t q_full;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
-    uint64_t s_full[2];
+    uint64_t s_full[3];                  // S of tile kt in TMEM buffer kt % 3
     uint64_t p_ready;
-    uint64_t o_done[2];                  // P.V of tile kt done -> o_done[kt & 1]
+    uint64_t o_done[3];                  // P.V of tile kt done -> o_done[kt % 3]
     uint64_t recv_full[2];               // local expect_tx + the peer's asynchronous stores (bytes)
     uint64_t can_send[2];                // arrived by the peer's 4 row warps after reading its recv[b]
     uint32_t tmem_base;
@@ -185,7 +186,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(&s.kv_full[i], 1);
             mbar_init(&s.kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 3; ++i) {
             mbar_init(&s.s_full[i], 1);
             mbar_init(&s.o_done[i], 1);
         }
@@ -205,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();          // both CTAs' barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
-    const uint32_t tmem_s[2] = {tmem, tmem + 64};
+    const uint32_t tmem_s[3] = {tmem, tmem + 64, tmem + 128};   // S / P buffers
     const uint32_t tmem_o = tmem + 256;
 
     if (warp == 4) {
@@ -250,20 +251,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int st = kt % kStages;
                 const uint32_t v_addr = smem_u32(s.kv[st][0]);
-                const uint32_t p_tmem = tmem_s[kt & 1];           // P (16-bit pairs) over the S columns
+                const uint32_t p_tmem = tmem_s[kt % 3];           // P (16-bit pairs) over the S columns
                 for (int ks = 0; ks < kN / 16; ++ks) {
                     const uint64_t b = smem_desc(v_addr + ks * 2048, kKBlk, 1024, kLayoutSwizzle128B);
                     mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
                 }
-                mma_commit(&s.o_done[kt & 1]);
+                mma_commit(&s.o_done[kt % 3]);
                 mma_commit(&s.kv_empty[st]);
                 return true;
             };
             for (int kt = 0; ok && kt < n_kt; ++kt) {
-                const int st = kt % kStages, sb = kt & 1;
+                const int st = kt % kStages, sb = kt % 3;
                 if (!mbar_wait(&s.kv_full[st], (kt / kStages) & 1)) { ok = false; break; }
-                // the buffer's previous tile (kt-2) must be through its P.V (P lives in it)
-                if (kt >= 2 && !mbar_wait(&s.o_done[sb], ((kt / 2) - 1) & 1)) { ok = false; break; }
+                // the buffer's previous tile (kt-3) must be through its P.V (P lives in it)
+                if (kt >= 3 && !mbar_wait(&s.o_done[sb], ((kt / 3) - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 for (int blk = 0; blk < nkb; ++blk)
                     for (int k = 0; k < 4; ++k) {
@@ -282,9 +283,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------- exchange / softmax / epilogue rows --
-        // Software pipeline: the partial scores of tile kt+1 are read from TMEM
-        // and sent to the peer before tile kt is combined, so the cross-SM
-        // exchange latency overlaps the previous tile's softmax.
+        // Per tile: read the partial scores from TMEM, send them to the peer
+        // (double-buffered receive, so the peer can run a tile ahead), add the
+        // peer's partial, softmax, P into TMEM.
         const int r = tid;
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
         uint32_t recv_peer[2], recv_full_peer[2], can_send_peer[2];
@@ -297,16 +298,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int sw = r & 15;                   // chunk swizzle of row r
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        float cur[kN], nxt[kN];
+        float cur[kN];
         // read partial scores of tile t from TMEM and send them to the peer's recv[t & 1]
         auto fetch_and_send = [&](int t, float (&sc)[kN]) -> bool {
             const int b = t & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&s.s_full[b], (t / 2) & 1))) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.s_full[t % 3], (t / 3) & 1))) return false;
             tc_fence_after();
 #pragma unroll
             for (int c = 0; c < kN; c += 16) {
                 uint32_t v[16];
-                tmem_ld16(tmem_s[b] + lane_off + c, v);
+                tmem_ld16(tmem_s[t % 3] + lane_off + c, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) sc[c + i] = __uint_as_float(v[i]);
@@ -319,15 +320,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             recv_full_peer[b]);
             return true;
         };
-        if (n_kt > 0) ok = fetch_and_send(0, cur);
         for (int kt = 0; ok && kt < n_kt; ++kt) {
-            const int sb = kt & 1;
+            const int sb = kt & 1;         // receive buffer
+            const int pb = kt % 3;         // S / P buffer
             const int64_t kbase = j0 + (int64_t)kt * kN;
             const int valid = (int)((j1 - kbase) < kN ? (j1 - kbase) : kN);
-            if (kt + 1 < n_kt) {
-                ok = fetch_and_send(kt + 1, nxt);
-                if (!ok) break;
-            }
+            ok = fetch_and_send(kt, cur);
+            if (!ok) break;
             ok = __all_sync(0xffffffffu, wait_cluster(&s.recv_full[sb], (kt / 2) & 1));
             if (!ok) break;
             const float *mine = &s.recv[sb][r * kN];
@@ -352,7 +351,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             // rescaling O needs the previous P.V finished (rare: the row max moved by > 2^8)
             if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(kt - 1) & 1], ((kt - 1) / 2) & 1));
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(kt - 1) % 3], ((kt - 1) / 3) & 1));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll 1
@@ -378,7 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     lsum += p0 + p1;
                     pk[i] = pack2<T>(p0, p1);
                 }
-                tmem_st16(tmem_s[sb] + lane_off + c / 2, pk);
+                tmem_st16(tmem_s[pb] + lane_off + c / 2, pk);
             }
             tmem_wait_st();
             l = l * alpha + lsum;
@@ -398,11 +397,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&s.p_ready);
-#pragma unroll
-            for (int c = 0; c < kN; ++c) cur[c] = nxt[c];
         }
         if (ok && n_kt > 0)
-            ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) & 1], ((n_kt - 1) / 2) & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) % 3], ((n_kt - 1) / 3) & 1));
         if (!ok) {
             atomicExch(&s.abort, 1);
             atomicCAS(prm.status, 0, PA_DEVICE_TIMEOUT_SOFTMAX);

@@ -12,7 +12,7 @@
 //   warp 4     TMA producer: Q once, then K/V tiles of 128 keys gathered
 //              page by page through the block table (one 16-row box per
 //              page and 64-column half, 128-byte swizzle);
-//   warp 5     MMA issuer: S = Q K^T into one of two TMEM buffers, then
+//   warp 5     MMA issuer: S = Q K^T into one of three TMEM buffers, then
 //              O += P V with P read from tensor memory: the softmax warps
 //              overwrite their row of the S buffer with P as 16-bit pairs.
 // K/V tiles use a 3-stage shared-memory ring; P never touches shared memory.
@@ -56,9 +56,9 @@ struct Smem {
     uint64_t q_full;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
-    uint64_t s_full[2];
+    uint64_t s_full[3];            // S of tile kt in TMEM buffer kt % 3
     uint64_t p_ready;
-    uint64_t o_done[2];            // P.V of tile kt done -> o_done[kt & 1]
+    uint64_t o_done[3];            // P.V of tile kt done -> o_done[kt % 3]
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -117,10 +117,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&s.kv_full[i], 1);
             mbar_init(&s.kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&s.s_full[i], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&s.s_full[i], 1);
         mbar_init(&s.p_ready, kM);
-        mbar_init(&s.o_done[0], 1);
-        mbar_init(&s.o_done[1], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&s.o_done[i], 1);
         s.abort = 0;
         fence_mbar_init();
     }
@@ -132,8 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
-    const uint32_t tmem_s[2] = {tmem, tmem + 128};
-    const uint32_t tmem_o = tmem + 256;
+    const uint32_t tmem_s[3] = {tmem, tmem + 128, tmem + 256};   // S / P buffers
+    const uint32_t tmem_o = tmem + 384;
 
     if (warp == 4) {
         // ---------------------------------------------------- TMA producer --
@@ -185,20 +184,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int st = kt % kStages;
                 const uint32_t v_addr = smem_u32(s.v[st]);
-                const uint32_t p_tmem = tmem_s[kt & 1];          // P (16-bit pairs) over the S columns
+                const uint32_t p_tmem = tmem_s[kt % 3];          // P (16-bit pairs) over the S columns
                 for (int ks = 0; ks < kN / 16; ++ks) {
                     const uint64_t b = smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, kLayoutSwizzle128B);
                     mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
                 }
-                mma_commit(&s.o_done[kt & 1]);
+                mma_commit(&s.o_done[kt % 3]);
                 mma_commit(&s.kv_empty[st]);
                 return true;
             };
-            for (int kt = 0; ok && kt < n_kt; ++kt) {
-                const int st = kt % kStages, sb = kt & 1;
-                if (!mbar_wait(&s.kv_full[st], (kt / kStages) & 1)) { ok = false; break; }
-                // the buffer's previous tile (kt-2) must be through its P.V (P lives in it)
-                if (kt >= 2 && !mbar_wait(&s.o_done[sb], ((kt / 2) - 1) & 1)) { ok = false; break; }
+            // S runs two tiles ahead of P.V: S0, S1, then per tile P.V(kt), S(kt+2).
+            auto issue_s = [&](int kt) -> bool {
+                const int st = kt % kStages, sb = kt % 3;
+                if (!mbar_wait(&s.kv_full[st], (kt / kStages) & 1)) return false;
+                // the buffer's previous tile (kt-3) must be through its P.V (P lives in it)
+                if (kt >= 3 && !mbar_wait(&s.o_done[sb], ((kt / 3) - 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t k_addr = smem_u32(s.k[st]);
                 for (int ks = 0; ks < kD / 16; ++ks) {
@@ -207,9 +207,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                smem_desc(k_addr + o, 16, 1024, kLayoutSwizzle128B), idesc_s, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&s.s_full[sb]);
-                if (kt > 0 && !issue_pv(kt - 1)) { ok = false; break; }
+                return true;
+            };
+            for (int kt = 0; ok && kt < 2 && kt < n_kt; ++kt) ok = issue_s(kt);
+            for (int kt = 0; ok && kt < n_kt; ++kt) {
+                ok = issue_pv(kt);
+                if (ok && kt + 2 < n_kt) ok = issue_s(kt + 2);
             }
-            if (ok && n_kt > 0) ok = issue_pv(n_kt - 1);
             if (!ok) set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_MMA);
         }
     } else {
@@ -221,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int kt = 0; kt < n_kt && ok; ++kt) {
-            const int sb = kt & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[sb], (kt / 2) & 1));
+            const int sb = kt % 3;
+            ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[sb], (kt / 3) & 1));
             if (!ok) break;
             tc_fence_after();
             const int kbase = kt * kN;
@@ -242,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // rescaling O needs the previous P.V finished (rare: the row max moved by > 2^8)
             if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(kt - 1) & 1], ((kt - 1) / 2) & 1));
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(kt - 1) % 3], ((kt - 1) / 3) & 1));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll 1
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&s.p_ready);
         }
         if (ok && n_kt > 0)
-            ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) & 1], ((n_kt - 1) / 2) & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) % 3], ((n_kt - 1) / 3) & 1));
         if (!ok) {
             set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_SOFTMAX);
         } else {
