@@ -159,6 +159,24 @@ int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32
 int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t num_sms);
 
 /*
+ * One decode step forward, on the device: every query of an uploaded plan
+ * moves to position pos + 1 of its sequence, its write slot is taken from the
+ * block table and its sequence length grows to cover the new position.  This
+ * keeps the per-step schedule in device memory, so a CUDA graph captured
+ * around pa_plan_advance + paged_kv_store + an attention call replays a
+ * decode loop step after step without re-capture (libmir-cuda 0.1.0,
+ * `CapturedDecodeAttentionBf16`; boostr 0.1.0, `DeviceScalars::update`: write
+ * at seq_len, attend over seq_len + 1, updated stream-ordered with no host
+ * synchronisation).  The caller reserves the pages ahead in the block table
+ * given to paged_attn_plan (entries past a sequence's current pages are not
+ * validated there).  A position the table does not map leaves that query
+ * unchanged and sets PA_DEVICE_RANGE in the device status word.  Plans with
+ * prefill tiles are refused (PA_ERR_STATE); the host copy advances with each
+ * call, but graph replays advance only the device copy.
+ */
+pa_status pa_plan_advance(pa_plan *plan, pa_stream_t stream);
+
+/*
  * Cache append (`DevicePlan::append_with_report`): for every query q and head
  * h, new_k[q, h, :] is copied bit-for-bit into k_cache[page, row, h, :] and
  * new_v[q, h, :] into v_cache[page, row, h, :], where page =
@@ -284,6 +302,7 @@ pa_status pa_time_next_kernel(void *start_event, void *stop_event);
 #define PA_DEVICE_TIMEOUT_TMA 1
 #define PA_DEVICE_TIMEOUT_MMA 2
 #define PA_DEVICE_TIMEOUT_SOFTMAX 3
+#define PA_DEVICE_RANGE 4
 pa_status pa_device_status(int32_t *code, int32_t clear);
 
 #ifdef __cplusplus

@@ -13,11 +13,13 @@ library's sm_103a kernels:
 """
 from ._binding import (EXPORTED, MAX_SPLITS, PagedAttentionError, Plan, device_status, lib_path, load,
                        make_workspace, paged_attn_forward, paged_attn_forward_split, paged_attn_plan,
+                       paged_attn_plan_advance,
                        paged_attn_split_heuristic, paged_kv_store, paged_mla_forward, paged_mla_split_heuristic,
                        time_next_kernel, workspace_bytes)
 from .buildlib import build
 
 __all__ = ["EXPORTED", "MAX_SPLITS", "PagedAttentionError", "Plan", "build", "device_status", "lib_path",
            "load", "make_workspace", "paged_attn_forward", "paged_attn_forward_split", "paged_attn_plan",
+           "paged_attn_plan_advance",
            "paged_attn_split_heuristic", "paged_kv_store", "paged_mla_forward", "paged_mla_split_heuristic",
            "time_next_kernel", "workspace_bytes"]

@@ -30,7 +30,8 @@ MAX_SPLITS = 64
 EXPORTED = ["pa_last_error", "pa_status_string", "pa_abi_version", "paged_attn_plan",
             "pa_plan_device_bytes", "pa_plan_upload", "pa_plan_destroy", "pa_plan_describe",
             "pa_workspace_bytes", "paged_attn_split_heuristic", "paged_mla_split_heuristic", "paged_kv_store", "paged_attn_forward",
-            "paged_attn_forward_split", "paged_mla_forward", "pa_time_next_kernel", "pa_device_status"]
+            "paged_attn_forward_split", "paged_mla_forward", "pa_plan_advance", "pa_time_next_kernel",
+            "pa_device_status"]
 
 
 class PagedAttentionError(RuntimeError):
@@ -87,6 +88,8 @@ def load() -> ctypes.CDLL:
     lib.paged_mla_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_float, i32,
                                       ctypes.c_int, vp, sz, i32, vp]
     lib.paged_mla_forward.restype = ctypes.c_int
+    lib.pa_plan_advance.argtypes = [vp, vp]
+    lib.pa_plan_advance.restype = ctypes.c_int
     lib.pa_time_next_kernel.argtypes = [vp, vp]
     lib.pa_time_next_kernel.restype = ctypes.c_int
     lib.pa_device_status.argtypes = [ctypes.POINTER(i32), i32]
@@ -334,6 +337,13 @@ def paged_mla_forward(plan: Plan, q, qp, latent_cache, pos_cache, scale: float, 
                                     float(scale), 1 if causal else 0, _DTYPES[dt], ws_ptr, ws_bytes,
                                     int(splits), _stream(dev)))
     return out
+
+
+def paged_attn_plan_advance(plan: Plan) -> None:
+    """Move every query of a decode plan one position forward, on the device (graph-capturable)."""
+    if plan.words is None:
+        raise ValueError("plan has not been uploaded")
+    _check(load().pa_plan_advance(plan.handle, _stream(plan.device)))
 
 
 def time_next_kernel(start: torch.cuda.Event, stop: torch.cuda.Event) -> None:

@@ -66,6 +66,9 @@ cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st);
 bool mla_supported(const AttnArgs &a);
 cudaError_t launch_mla(const AttnArgs &a, bool use_decode_list, cudaStream_t st);
 
+// One decode step forward on the device (pa_plan_advance).
+cudaError_t launch_plan_advance(const PlanView &plan, int32_t *status, cudaStream_t st);
+
 // Device status word (bounded waits record their timeouts here).
 cudaError_t read_device_status(int32_t *code, bool clear);
 // Device address of the status word on the current device (cached per device).

@@ -224,8 +224,10 @@ pa_status paged_attn_plan(const int32_t *seq_lens, int32_t num_seqs, const int32
         m[3] = 0;
     }
     if (num_seqs) std::memcpy(w + p->off_seqlen, seq_lens, sizeof(int32_t) * (size_t)num_seqs);
-    for (int64_t e = 0; e < (int64_t)num_seqs * width; ++e)
-        w[p->off_table + e] = block_table[e] < 0 ? 0 : block_table[e];  // unused entries never read
+    // Entries past a sequence's pages are kept as given (e.g. -1, or pages
+    // reserved ahead for pa_plan_advance); the attention kernels never read them.
+    if ((int64_t)num_seqs * width > 0)
+        std::memcpy(w + p->off_table, block_table, sizeof(int32_t) * (size_t)num_seqs * width);
     if (!decode.empty()) std::memcpy(w + p->off_decode, decode.data(), sizeof(int32_t) * decode.size());
     if (!tiles.empty()) std::memcpy(w + p->off_tiles, tiles.data(), sizeof(int32_t) * tiles.size());
     {
@@ -441,6 +443,33 @@ pa_status paged_mla_forward(const pa_plan *plan, const void *q, const void *qp, 
     return attention(plan, q, latent_cache, latent_cache, qp, pos_cache, out, num_heads, 1, latent_dim,
                      latent_dim, pos_dim, scale, causal, dtype, workspace, workspace_bytes, splits, true, true,
                      (cudaStream_t)stream, "paged_mla_forward");
+}
+
+pa_status pa_plan_advance(pa_plan *plan, pa_stream_t stream) {
+    if (!plan) return fail(PA_ERR_ARG, "pa_plan_advance: plan is null");
+    if (plan->n_tiles > 0)
+        return fail(PA_ERR_STATE, "pa_plan_advance: plans with prefill tiles cannot advance");
+    if (plan->queries == 0) return PA_OK;
+    if (!plan->dev) return fail(PA_ERR_STATE, "pa_plan_advance: plan not uploaded");
+    int32_t *status = pa::device_status_ptr();
+    if (!status) return fail(PA_ERR_CUDA, "pa_plan_advance: device status word unavailable");
+    cudaError_t e = pa::launch_plan_advance(view_of(plan), status, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(e, "pa_plan_advance launch");
+    // keep the host copy in step with one advance (graph replays advance only the device copy)
+    int32_t *w = plan->words.data();
+    for (int32_t q = 0; q < plan->queries; ++q) {
+        int32_t *m = w + plan->off_qmeta + 4 * (size_t)q;
+        const int64_t np = (int64_t)m[1] + 1;
+        if (np >= (int64_t)plan->width * plan->page_size) continue;
+        const int32_t pg = w[plan->off_table + (size_t)m[0] * plan->width + np / plan->page_size];
+        if (pg < 0 || pg >= plan->pages) continue;
+        m[1] = (int32_t)np;
+        m[2] = pg * plan->page_size + (int32_t)(np % plan->page_size);
+        int32_t &sl = w[plan->off_seqlen + m[0]];
+        if (sl < np + 1) sl = (int32_t)(np + 1);
+        plan->max_seq_len = std::max<int64_t>(plan->max_seq_len, sl);
+    }
+    return PA_OK;
 }
 
 pa_status pa_time_next_kernel(void *start_event, void *stop_event) {

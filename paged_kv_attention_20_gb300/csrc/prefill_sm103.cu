@@ -7,12 +7,13 @@
 // sees keys 0..p_i: the cached context plus the chunk's earlier rows.
 //
 // One CTA per (tile of up to 128 consecutive queries, query head):
-//   warps 0-3  softmax / O correction / epilogue, thread r owns query row r
-//              (TMEM lane r);
-//   warp 4     TMA producer: Q once, then K/V tiles of 128 keys gathered
+//   warps 0-7  softmax / O correction / epilogue: query row r (TMEM lane r) is
+//              shared by warps r/32 and r/32+4, each taking 64 of the 128 key
+//              (and output) columns; row maxima and sums cross over shared memory;
+//   warp 8     TMA producer: Q once, then K/V tiles of 128 keys gathered
 //              page by page through the block table (one 16-row box per
 //              page and 64-column half, 128-byte swizzle);
-//   warp 5     MMA issuer: S = Q K^T into one of three TMEM buffers, then
+//   warp 9     MMA issuer: S = Q K^T into one of three TMEM buffers, then
 //              O += P V with P read from tensor memory: the softmax warps
 //              overwrite their row of the S buffer with P as 16-bit pairs.
 // K/V tiles use a 3-stage shared-memory ring; P never touches shared memory.
@@ -42,7 +43,7 @@ constexpr int kM = 128;          // queries per tile (TMEM lanes)
 constexpr int kN = 128;          // keys per tile
 constexpr int kD = 128;          // head dim (== value dim)
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;        // 8 softmax warps + producer + MMA issuer
 constexpr uint32_t kHalfBytes = kM * 128;          // one 64-column half of a 128-row tile
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;    // 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
@@ -59,6 +60,8 @@ struct Smem {
     uint64_t s_full[3];            // S of tile kt in TMEM buffer kt % 3
     uint64_t p_ready;
     uint64_t o_done[3];            // P.V of tile kt done -> o_done[kt % 3]
+    float xred[2 * kM];            // row-max / row-sum exchange between the two warps of a row
+    uint64_t xa[4], xb[4];         // per lane quarter: values written / values read
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -118,7 +121,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&s.kv_empty[i], 1);
         }
         for (int i = 0; i < 3; ++i) mbar_init(&s.s_full[i], 1);
-        mbar_init(&s.p_ready, kM);
+        mbar_init(&s.p_ready, 2 * kM);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&s.xa[i], 64);
+            mbar_init(&s.xb[i], 64);
+        }
         for (int i = 0; i < 3; ++i) mbar_init(&s.o_done[i], 1);
         s.abort = 0;
         fence_mbar_init();
@@ -134,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_s[3] = {tmem, tmem + 128, tmem + 256};   // S / P buffers
     const uint32_t tmem_o = tmem + 384;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ---------------------------------------------------- TMA producer --
         // Lane 0 owns the barriers; lanes 0..pages_per_tile-1 each gather one
         // page of K and V (4 boxes), so the box issue runs 8 lanes wide.
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(s.v[st] + kHalfBytes + off, &tm_v, 64, kvh, row, &s.kv_full[st]);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------ MMA issuer --
         if (lane == 0) {
             const uint32_t idesc_s = idesc_f16(kM, kN, prm.bf16 != 0, false, false);
@@ -218,27 +225,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------- softmax / correction rows --
-        const int r = tid;                       // query row == TMEM lane
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        // Warps w and w+4 share TMEM lanes 32*(w%4).. (query rows); warp w takes
+        // key/value columns 0..63 of its rows and warp w+4 columns 64..127.
+        const int q4 = warp & 3, h2 = warp >> 2;
+        const int r = 32 * q4 + lane;            // query row == TMEM lane
+        const int col0 = 64 * h2;
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         const int my_pos = pos0 + r;
         const int vis_end = prm.causal ? min(my_pos + 1, seq_len) : seq_len;  // keys [0, vis_end)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
+        int xphase = 0;
+        // value of the other warp of this row (bounded waits; false on timeout)
+        auto exchange = [&](float v, float &other) -> bool {
+            if (xphase > 0 && !__all_sync(0xffffffffu, mbar_wait(&s.xb[q4], (xphase - 1) & 1))) return false;
+            s.xred[h2 * kM + r] = v;
+            mbar_arrive(&s.xa[q4]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.xa[q4], xphase & 1))) return false;
+            other = s.xred[(1 - h2) * kM + r];
+            mbar_arrive(&s.xb[q4]);
+            ++xphase;
+            return true;
+        };
         for (int kt = 0; kt < n_kt && ok; ++kt) {
             const int sb = kt % 3;
             ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[sb], (kt / 3) & 1));
             if (!ok) break;
             tc_fence_after();
-            const int kbase = kt * kN;
-            // the row's 128 scores into registers (four loads, one wait)
-            uint32_t sv[kN];
-#pragma unroll
-            for (int c = 0; c < kN; c += 32) tmem_ld32(tmem_s[sb] + lane_off + c, sv + c);
+            const int kbase = kt * kN + col0;
+            // my 64 scores of the row into registers (two loads, one wait)
+            uint32_t sv[64];
+            tmem_ld32(tmem_s[sb] + lane_off + col0, sv);
+            tmem_ld32(tmem_s[sb] + lane_off + col0 + 32, sv + 32);
             tmem_wait_ld();
-            float mt = -INFINITY;
+            float mine = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kN; ++c)
-                if (kbase + c < vis_end) mt = fmaxf(mt, __uint_as_float(sv[c]) * prm.scale_log2);
+            for (int c = 0; c < 64; ++c)
+                if (kbase + c < vis_end) mine = fmaxf(mine, __uint_as_float(sv[c]) * prm.scale_log2);
+            float other;
+            ok = exchange(mine, other);
+            if (!ok) break;
+            const float mt = fmaxf(mine, other);
             float alpha = 1.f;
             if (mt > m_ref + kSlack) {
                 alpha = exp2f(m_ref - mt);
@@ -250,48 +277,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < kD; c += 16) {
+                for (int c = 0; c < 64; c += 16) {
                     uint32_t v[16];
-                    tmem_ld16(tmem_o + lane_off + c, v);
+                    tmem_ld16(tmem_o + lane_off + col0 + c, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tmem_st16(tmem_o + lane_off + c, v);
+                    tmem_st16(tmem_o + lane_off + col0 + c, v);
                 }
                 tmem_wait_st();
             }
-            // P = exp2(s - m_ref) as 16-bit pairs, written over this row's S columns
-            // (each 32-score chunk is re-read from TMEM before its P overwrites it)
+            // P = exp2(s - m_ref) as 16-bit pairs over my S columns (already in registers)
             float lsum = 0.f;
-#pragma unroll 1
-            for (int c = 0; c < kN; c += 32) {
-                uint32_t sc[32], pk[16];
-                tmem_ld32(tmem_s[sb] + lane_off + c, sc);
-                tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 64; c += 32) {
+                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int k0 = kbase + c + 2 * i;
-                    const float p0 = k0 < vis_end ? exp2f(__uint_as_float(sc[2 * i]) * prm.scale_log2 - m_ref) : 0.f;
-                    const float p1 = k0 + 1 < vis_end ? exp2f(__uint_as_float(sc[2 * i + 1]) * prm.scale_log2 - m_ref) : 0.f;
+                    const float p0 = k0 < vis_end ? exp2f(__uint_as_float(sv[c + 2 * i]) * prm.scale_log2 - m_ref) : 0.f;
+                    const float p1 = k0 + 1 < vis_end ? exp2f(__uint_as_float(sv[c + 2 * i + 1]) * prm.scale_log2 - m_ref) : 0.f;
                     lsum += p0 + p1;
                     pk[i] = pack2<T>(p0, p1);
                 }
-                tmem_st16(tmem_s[sb] + lane_off + c / 2, pk);
+                tmem_st16(tmem_s[sb] + lane_off + (col0 + c) / 2, pk);
             }
             tmem_wait_st();
             l = l * alpha + lsum;
             // V rows at or past the sequence end (tail slots) must not reach the MMA
-            if (kbase + kN > seq_len) {
+            if (kt * kN + kN > seq_len) {
                 const int st = kt % kStages;
                 ok = __all_sync(0xffffffffu, mbar_wait(&s.kv_full[st], (kt / kStages) & 1));
                 if (!ok) break;
-                if (kbase + r >= seq_len) {
-                    uint4 z = make_uint4(0, 0, 0, 0);
+                if (kt * kN + r >= seq_len) {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        *reinterpret_cast<uint4 *>(s.v[st] + r * 128 + i * 16) = z;
-                        *reinterpret_cast<uint4 *>(s.v[st] + kHalfBytes + r * 128 + i * 16) = z;
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<uint4 *>(s.v[st] + h2 * kHalfBytes + r * 128 + i * 16) = z;
                 }
             }
             fence_proxy_async_smem();      // zeroed V rows (if any) before the tensor core reads them
@@ -300,17 +322,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && n_kt > 0)
             ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) % 3], ((n_kt - 1) / 3) & 1));
+        float l_other = 0.f;
+        if (ok) ok = exchange(l, l_other);
         if (!ok) {
             set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_SOFTMAX);
         } else {
             // every lane loads (warp-collective); only rows of real queries store
             tc_fence_after();
-            const float inv = 1.f / l;
-            T *dst = static_cast<T *>(prm.out) + ((int64_t)(q0 + r) * prm.hq + h) * kD;
+            const float inv = 1.f / (l + l_other);
+            T *dst = static_cast<T *>(prm.out) + ((int64_t)(q0 + r) * prm.hq + h) * kD + col0;
 #pragma unroll 1
-            for (int c = 0; c < kD; c += 16) {
+            for (int c = 0; c < 64; c += 16) {
                 uint32_t v[16];
-                tmem_ld16(tmem_o + lane_off + c, v);
+                tmem_ld16(tmem_o + lane_off + col0 + c, v);
                 tmem_wait_ld();
                 uint4 w0, w1;
                 w0.x = pack2<T>(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);

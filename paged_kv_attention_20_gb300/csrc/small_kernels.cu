@@ -123,6 +123,35 @@ cudaError_t launch_merge(const AttnArgs &a, bool use_list, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// Every query moves to the next position of its sequence: pos + 1, the write
+// slot of that position from the block table, and a sequence length covering
+// it.  A position the table does not map (past the row, or a negative or
+// out-of-pool entry) leaves the query unchanged and records PA_DEVICE_RANGE.
+__global__ void plan_advance_kernel(PlanView plan, int32_t *status) {
+    const int q = blockIdx.x * blockDim.x + threadIdx.x;
+    if (q >= plan.queries) return;
+    int4 *meta = const_cast<int4 *>(plan.qmeta) + q;
+    const int4 m = *meta;
+    const int64_t np = (int64_t)m.y + 1;
+    if (np >= (int64_t)plan.width * plan.page_size) {
+        atomicCAS(status, 0, PA_DEVICE_RANGE);
+        return;
+    }
+    const int32_t pg = plan.table[(int64_t)m.x * plan.width + np / plan.page_size];
+    if (pg < 0 || pg >= plan.pages) {
+        atomicCAS(status, 0, PA_DEVICE_RANGE);
+        return;
+    }
+    *meta = make_int4(m.x, (int)np, pg * plan.page_size + (int)(np % plan.page_size), 0);
+    atomicMax(const_cast<int32_t *>(plan.seq_lens) + m.x, (int)(np + 1));
+}
+
+cudaError_t launch_plan_advance(const PlanView &plan, int32_t *status, cudaStream_t st) {
+    const int threads = 128;
+    plan_advance_kernel<<<(plan.queries + threads - 1) / threads, threads, 0, st>>>(plan, status);
+    return cudaGetLastError();
+}
+
 int32_t *device_status_ptr() {
     static int32_t *cached[64] = {nullptr};
     int dev = 0;

@@ -158,3 +158,15 @@ def test_zero_queries_is_ok_without_launch(built_lib):
     fake = ctypes.c_void_p(0x1000)
     assert lib.paged_attn_forward(p.handle, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, None) == 0
     assert lib.paged_kv_store(p.handle, fake, fake, fake, fake, 1, 64, 64, 2, None) == 0
+
+
+def test_plan_advance_refusals(built_lib):
+    lib = _lib()
+    # a plan with a prefill run (>= 16 consecutive positions) cannot advance
+    p = plan([40], [[0, 1, 2]], [0] * 20, list(range(20)), 16, 3)
+    assert p.n_tiles == 1
+    assert lib.pa_plan_advance(p.handle, None) == 10
+    # a decode plan must be uploaded first
+    d = plan([5], [[0]], [0], [4], 16, 1)
+    assert lib.pa_plan_advance(d.handle, None) == 10
+    assert lib.pa_plan_advance(None, None) == 1
