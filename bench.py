@@ -536,8 +536,7 @@ def main():
     kern_mean = statistics.mean(kern_ms)
     achieved = kvb / (kern_mean / 1e3) / 1e9
     traffic = profile_traffic("decode_tma_gqa_decode_bf16",
-                              ["paged_kv_attention_20_gb300/csrc/decode_tma.cu",
-                               "paged_kv_attention_20_gb300/csrc/small_kernels.cu"])
+                              ["paged_kv_attention_20_gb300/csrc/decode_tma.cu"])
 
     if rank != 0:
         barrier(world)

@@ -393,8 +393,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4 *>(s.kv[st][blk] + r * 128 + i * 16) = z;
                 }
+                fence_proxy_async_smem();  // the zeroed rows before the tensor core reads them
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&s.p_ready);
         }

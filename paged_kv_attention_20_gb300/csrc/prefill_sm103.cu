@@ -315,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 8; ++i)
                         *reinterpret_cast<uint4 *>(s.v[st] + h2 * kHalfBytes + r * 128 + i * 16) = z;
                 }
+                fence_proxy_async_smem();  // the zeroed V rows before the tensor core reads them
             }
-            fence_proxy_async_smem();      // zeroed V rows (if any) before the tensor core reads them
             tc_fence_before();
             mbar_arrive(&s.p_ready);
         }
