@@ -115,6 +115,16 @@ __device__ __forceinline__ void arrive_remote(uint32_t remote_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(remote_bar) : "memory");
 }
 
+// Relaxed remote arrive (no cluster-scope fence) used to say "my receive
+// buffer has been read".  `dep` is a value computed from everything that was
+// read, so the arrive is issued only after those loads have returned.
+__device__ __forceinline__ void arrive_remote_after(uint32_t remote_bar, float dep) {
+    asm volatile("{\n .reg .b32 d;\n mov.b32 d, %1;\n mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n}\n" ::"r"(
+                     remote_bar),
+                 "f"(dep)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool try_wait_cluster(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -335,8 +345,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float4 o = *reinterpret_cast<const float4 *>(mine + ((c ^ sw) * 4));
                 cur[4 * c] += o.x; cur[4 * c + 1] += o.y; cur[4 * c + 2] += o.z; cur[4 * c + 3] += o.w;
             }
-            __syncwarp();
-            if (lane == 0) arrive_remote(can_send_peer[sb]);   // this warp's rows of recv[sb] are read
             // online softmax (identical on both CTAs)
             float mt = -INFINITY;
 #pragma unroll
@@ -344,6 +352,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 cur[c] = c < valid ? cur[c] * prm.scale_log2 : -INFINITY;
                 mt = fmaxf(mt, cur[c]);
             }
+            // this warp's rows of recv[sb] are read (mt depends on every loaded value)
+            const float wdep = __shfl_sync(0xffffffffu, mt, 0) + __shfl_sync(0xffffffffu, mt, 31);
+            if (lane == 0) arrive_remote_after(can_send_peer[sb], wdep);
             float alpha = 1.f;
             if (mt > m_ref + kSlack) {
                 alpha = exp2f(m_ref - mt);
