@@ -44,7 +44,7 @@ constexpr int kHeads = 128;               // M: heads per cluster (TMEM lanes)
 constexpr int kR = 512;                   // latent rank
 constexpr int kP = 64;                    // rotary position dims
 constexpr int kN = 64;                    // keys per tile
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kThreads = 192;
 constexpr int kBlk = kHeads * 128;        // one 64-column block of the Q tile (bytes)
 constexpr int kKBlk = kN * 128;           // one 64-column block of a key tile (bytes)
@@ -53,15 +53,16 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kSlack = 8.f;
 
 struct Smem {
-    uint8_t q[5][kBlk];                  // own Q blocks (rank 0: q[0:256] + qp; rank 1: q[256:512])
+    uint8_t qp[kBlk];                    // rank 0: position Q block (the latent part of Q lives in TMEM)
     uint8_t kv[kStages][5][kKBlk];       // own latent blocks 0..3 (+ position block 4 on rank 0)
     float recv[2][kHeads * kN];          // peer's partial scores, double buffered, 16-byte chunks XOR-swizzled
-    uint64_t q_full;
+    uint64_t q_full;                     // rank 0: position Q block landed
+    uint64_t q_ready;                    // latent Q rows stored in TMEM by the row threads
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
-    uint64_t s_full[3];                  // S of tile kt in TMEM buffer kt % 3
+    uint64_t s_full[2];                  // S of tile kt in TMEM buffer kt % 2
     uint64_t p_ready;
-    uint64_t o_done[3];                  // P.V of tile kt done -> o_done[kt % 3]
+    uint64_t o_done[2];                  // P.V of tile kt done -> o_done[kt % 2]
     uint64_t recv_full[2];               // local expect_tx + the peer's asynchronous stores (bytes)
     uint64_t can_send[2];                // arrived by the peer's 4 row warps after reading its recv[b]
     uint32_t tmem_base;
@@ -72,6 +73,7 @@ constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
 struct MlaParams {
     PlanView plan;
+    const void *q;          // absorbed Q [queries, H, 512]
     void *out;
     float *ws_o, *ws_lse;
     int32_t *status;
@@ -171,7 +173,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
-    const int nkb = rank == 0 ? 5 : 4;     // K blocks this CTA contracts
 
     // cluster -> (item, head block, split)
     const int cl = blockIdx.x >> 1;
@@ -192,11 +193,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(&s.q_full, 1);
+        mbar_init(&s.q_ready, kHeads);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&s.kv_full[i], 1);
             mbar_init(&s.kv_empty[i], 1);
         }
-        for (int i = 0; i < 3; ++i) {
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s.s_full[i], 1);
             mbar_init(&s.o_done[i], 1);
         }
@@ -216,7 +218,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();          // both CTAs' barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
-    const uint32_t tmem_s[3] = {tmem, tmem + 64, tmem + 128};   // S / P buffers
+    const uint32_t tmem_q = tmem;                                 // latent Q: 256 x 16-bit = 128 columns
+    const uint32_t tmem_s[2] = {tmem + 128, tmem + 192};          // S / P buffers
     const uint32_t tmem_o = tmem + 256;
 
     if (warp == 4) {
@@ -224,10 +227,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_lat);
-            mbar_arrive_expect_tx(&s.q_full, (uint32_t)nkb * kBlk);
-            for (int b = 0; b < 4; ++b)
-                tma_load_3d(s.q[b], &tm_q, (int)(rank * 4 + b) * 64, hb * kHeads, qi, &s.q_full);
-            if (rank == 0) tma_load_3d(s.q[4], &tm_qp, 0, hb * kHeads, qi, &s.q_full);
+            if (rank == 0) {
+                mbar_arrive_expect_tx(&s.q_full, kBlk);
+                tma_load_3d(s.qp, &tm_qp, 0, hb * kHeads, qi, &s.q_full);
+            }
             const int used_pages = (seq_len + ps - 1) >> prm.ps_shift;
             const int oob_row = prm.plan.pages * ps;
             for (int kt = 0; kt < n_kt; ++kt) {
@@ -237,7 +240,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     atomicCAS(prm.status, 0, PA_DEVICE_TIMEOUT_TMA);
                     break;
                 }
-                mbar_arrive_expect_tx(&s.kv_full[st], (uint32_t)nkb * kKBlk);
+                mbar_arrive_expect_tx(&s.kv_full[st], (uint32_t)(rank == 0 ? 5 : 4) * kKBlk);
                 const int64_t jt = j0 + (int64_t)kt * kN;
                 for (int b = 0; b < kN; b += prm.box_rows) {
                     const int64_t j = jt + b;
@@ -255,32 +258,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc_s = idesc_f16(kHeads, kN, prm.bf16 != 0, false, false);
             const uint32_t idesc_o = idesc_f16(kHeads, 256, prm.bf16 != 0, false, true);
-            bool ok = mbar_wait(&s.q_full, 0);
+            bool ok = (rank != 0 || mbar_wait(&s.q_full, 0)) && mbar_wait(&s.q_ready, 0);
             auto issue_pv = [&](int kt) -> bool {
                 if (!mbar_wait(&s.p_ready, kt & 1)) return false;
                 tc_fence_after();
                 const int st = kt % kStages;
                 const uint32_t v_addr = smem_u32(s.kv[st][0]);
-                const uint32_t p_tmem = tmem_s[kt % 3];           // P (16-bit pairs) over the S columns
+                const uint32_t p_tmem = tmem_s[kt & 1];           // P (16-bit pairs) over the S columns
                 for (int ks = 0; ks < kN / 16; ++ks) {
                     const uint64_t b = smem_desc(v_addr + ks * 2048, kKBlk, 1024, kLayoutSwizzle128B);
                     mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
                 }
-                mma_commit(&s.o_done[kt % 3]);
+                mma_commit(&s.o_done[kt & 1]);
                 mma_commit(&s.kv_empty[st]);
                 return true;
             };
             for (int kt = 0; ok && kt < n_kt; ++kt) {
-                const int st = kt % kStages, sb = kt % 3;
+                const int st = kt % kStages, sb = kt & 1;
                 if (!mbar_wait(&s.kv_full[st], (kt / kStages) & 1)) { ok = false; break; }
-                // the buffer's previous tile (kt-3) must be through its P.V (P lives in it)
-                if (kt >= 3 && !mbar_wait(&s.o_done[sb], ((kt / 3) - 1) & 1)) { ok = false; break; }
+                // the buffer's previous tile (kt-2) must be through its P.V (P lives in it)
+                if (kt >= 2 && !mbar_wait(&s.o_done[sb], ((kt / 2) - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                for (int blk = 0; blk < nkb; ++blk)
+                for (int blk = 0; blk < 4; ++blk)            // latent columns: A from TMEM
                     for (int k = 0; k < 4; ++k) {
-                        const uint64_t a = smem_desc(smem_u32(s.q[blk]) + k * 32, 16, 1024, kLayoutSwizzle128B);
                         const uint64_t b = smem_desc(smem_u32(s.kv[st][blk]) + k * 32, 16, 1024, kLayoutSwizzle128B);
-                        mma_f16_ss(tmem_s[sb], a, b, idesc_s, (blk > 0 || k > 0) ? 1u : 0u);
+                        mma_f16_ts(tmem_s[sb], tmem_q + blk * 32 + k * 8, b, idesc_s, (blk > 0 || k > 0) ? 1u : 0u);
+                    }
+                if (rank == 0)                                   // position columns: A from shared memory
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t a = smem_desc(smem_u32(s.qp) + k * 32, 16, 1024, kLayoutSwizzle128B);
+                        const uint64_t b = smem_desc(smem_u32(s.kv[st][4]) + k * 32, 16, 1024, kLayoutSwizzle128B);
+                        mma_f16_ss(tmem_s[sb], a, b, idesc_s, 1u);
                     }
                 mma_commit(&s.s_full[sb]);
                 if (kt > 0 && !issue_pv(kt - 1)) { ok = false; break; }
@@ -306,18 +314,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             can_send_peer[b] = peer_addr(smem_u32(&s.can_send[b]), peer);
         }
         const int sw = r & 15;                   // chunk swizzle of row r
+        {
+            // latent Q row (this CTA's 256 columns) into TMEM as 16-bit pairs; rows past H are zero
+            const int h = hb * kHeads + r;
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const T *>(prm.q) +
+                                                               ((int64_t)qi * prm.heads + h) * kR + rank * 256);
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 16) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 v = h < prm.heads ? src[c / 4 + i] : make_uint4(0, 0, 0, 0);
+                    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+                }
+                tmem_st16(tmem_q + lane_off + c, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&s.q_ready);
+        }
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         float cur[kN];
         // read partial scores of tile t from TMEM and send them to the peer's recv[t & 1]
         auto fetch_and_send = [&](int t, float (&sc)[kN]) -> bool {
             const int b = t & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&s.s_full[t % 3], (t / 3) & 1))) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.s_full[t & 1], (t / 2) & 1))) return false;
             tc_fence_after();
 #pragma unroll
             for (int c = 0; c < kN; c += 16) {
                 uint32_t v[16];
-                tmem_ld16(tmem_s[t % 3] + lane_off + c, v);
+                tmem_ld16(tmem_s[t & 1] + lane_off + c, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) sc[c + i] = __uint_as_float(v[i]);
@@ -332,7 +359,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         };
         for (int kt = 0; ok && kt < n_kt; ++kt) {
             const int sb = kt & 1;         // receive buffer
-            const int pb = kt % 3;         // S / P buffer
+            const int pb = kt & 1;         // S / P buffer
             const int64_t kbase = j0 + (int64_t)kt * kN;
             const int valid = (int)((j1 - kbase) < kN ? (j1 - kbase) : kN);
             ok = fetch_and_send(kt, cur);
@@ -362,7 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             // rescaling O needs the previous P.V finished (rare: the row max moved by > 2^8)
             if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(kt - 1) % 3], ((kt - 1) / 3) & 1));
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(kt - 1) & 1], ((kt - 1) / 2) & 1));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll 1
@@ -410,7 +437,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_arrive(&s.p_ready);
         }
         if (ok && n_kt > 0)
-            ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) % 3], ((n_kt - 1) / 3) & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) & 1], ((n_kt - 1) / 2) & 1));
         if (!ok) {
             atomicExch(&s.abort, 1);
             atomicCAS(prm.status, 0, PA_DEVICE_TIMEOUT_SOFTMAX);
@@ -498,6 +525,7 @@ cudaError_t launch_mla(const AttnArgs &a, bool use_list, cudaStream_t st) {
     const int ps = a.plan.page_size;
     MlaParams prm{};
     prm.plan = a.plan;
+    prm.q = a.q;
     prm.out = a.out;
     prm.ws_o = a.ws_o;
     prm.ws_lse = a.ws_lse;
