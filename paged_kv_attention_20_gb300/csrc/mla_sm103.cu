@@ -19,10 +19,15 @@
 // the K-major B operand of Q.K^T and the MN-major B operand of P.V.
 //
 // Roles per CTA: warps 0-3 exchange/softmax/epilogue (thread r = head r, TMEM
-// lane r), warp 4 TMA producer (64-key tiles, 2 stages), warp 5 MMA issuer.
-// P (16-bit) is written back over its row of the S buffer in TMEM and read
-// from there by the P.V MMA; three S/P buffers let S of the next tile be
-// computed while the current tile's P waits for its P.V.
+// lane r), warp 4 TMA producer (64-key tiles, 3 stages), warp 5 MMA issuer.
+// The CTA's 256 latent columns of Q live in TMEM (the A operand of Q.K^T is
+// read from there), which leaves shared memory for three latent stages; the
+// 64 position columns of Q stay in shared memory on CTA 0.  P (16-bit) is
+// written back over its row of the S buffer in TMEM and read from there by
+// the P.V MMA; two S/P buffers let S of the next tile be computed while the
+// current tile's P waits for its P.V.  The peer's partial scores arrive by
+// asynchronous remote stores that complete bytes on a local mbarrier, into a
+// double-buffered, 16-byte-chunk-swizzled receive area.
 // Key tiles are one page at page_size 64 (several boxes for smaller pages).
 // Keys at or past the sequence end are masked and their latent rows zeroed
 // before P.V.  All waits are bounded (timeout -> device status word).
@@ -166,7 +171,7 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) 
 
 template <typename T>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
+    mla_kernel(const __grid_constant__ CUtensorMap tm_qp,
                const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_kp,
                MlaParams prm) {
     extern __shared__ uint8_t smem_raw[];
@@ -225,7 +230,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 4) {
         // ---------------------------------------------------- TMA producer --
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_lat);
             if (rank == 0) {
                 mbar_arrive_expect_tx(&s.q_full, kBlk);
@@ -540,11 +544,9 @@ cudaError_t launch_mla(const AttnArgs &a, bool use_list, cudaStream_t st) {
     prm.causal = a.causal;
     prm.bf16 = bf16 ? 1 : 0;
     const uint64_t rows = (uint64_t)a.plan.pages * ps;
-    CUtensorMap tq, tqp, tlat, tkp;
-    // Q [queries, H, 512] and QP [queries, H, 64]: boxes of 64 columns x 128 heads x 1 query
-    if (!encode_map_3d(&tq, a.q, bf16, kR, a.hq, a.plan.queries, (uint64_t)kR * 2, (uint64_t)kR * 2 * a.hq, 64,
-                       kHeads, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_map_3d(&tqp, a.qp, bf16, kP, a.hq, a.plan.queries, (uint64_t)kP * 2, (uint64_t)kP * 2 * a.hq, 64,
+    CUtensorMap tqp, tlat, tkp;
+    // QP [queries, H, 64]: boxes of 64 columns x 128 heads x 1 query (latent Q is read by the row threads)
+    if (!encode_map_3d(&tqp, a.qp, bf16, kP, a.hq, a.plan.queries, (uint64_t)kP * 2, (uint64_t)kP * 2 * a.hq, 64,
                        kHeads, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
         // latent [rows, 512] and position cache [rows, 64]: boxes of 64 columns x box_rows keys
         !encode_map_2d(&tlat, a.k, bf16, kR, rows, (uint64_t)kR * 2, 64, prm.box_rows,
@@ -562,7 +564,7 @@ cudaError_t launch_mla(const AttnArgs &a, bool use_list, cudaStream_t st) {
             if (e != cudaSuccess) return e;
             cfg = true;
         }
-        mla_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(tq, tqp, tlat, tkp, prm);
+        mla_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(tqp, tlat, tkp, prm);
     } else {
         static bool cfg = false;
         if (!cfg) {
@@ -570,7 +572,7 @@ cudaError_t launch_mla(const AttnArgs &a, bool use_list, cudaStream_t st) {
             if (e != cudaSuccess) return e;
             cfg = true;
         }
-        mla_kernel<__half><<<grid, kThreads, kSmemBytes, st>>>(tq, tqp, tlat, tkp, prm);
+        mla_kernel<__half><<<grid, kThreads, kSmemBytes, st>>>(tqp, tlat, tkp, prm);
     }
     return cudaGetLastError();
 }
