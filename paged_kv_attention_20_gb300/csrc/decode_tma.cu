@@ -33,19 +33,12 @@ using tc::mbar_arrive_expect_tx;
 using tc::mbar_init;
 using tc::mbar_wait;
 using tc::smem_u32;
+using tc::ffma2;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kSlack = 8.f;
 
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    unsigned long long r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;\n"
-        : "=l"(r)
-        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)),
-          "l"(*reinterpret_cast<unsigned long long *>(&c)));
-    return *reinterpret_cast<float2 *>(&r);
-}
 
 template <typename T> __device__ __forceinline__ float2 unpack2(uint32_t w);
 template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {

@@ -224,7 +224,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
     const uint32_t tmem_q = tmem;                                 // latent Q: 256 x 16-bit = 128 columns
-    const uint32_t tmem_s[2] = {tmem + 128, tmem + 192};          // S / P buffers
+    auto tmem_s = [tmem](int b) -> uint32_t { return tmem + 128u + 64u * (uint32_t)b; };   // S / P buffers 0, 1
     const uint32_t tmem_o = tmem + 256;
 
     if (warp == 4) {
@@ -268,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int st = kt % kStages;
                 const uint32_t v_addr = smem_u32(s.kv[st][0]);
-                const uint32_t p_tmem = tmem_s[kt & 1];           // P (16-bit pairs) over the S columns
+                const uint32_t p_tmem = tmem_s(kt & 1);           // P (16-bit pairs) over the S columns
                 for (int ks = 0; ks < kN / 16; ++ks) {
                     const uint64_t b = smem_desc(v_addr + ks * 2048, kKBlk, 1024, kLayoutSwizzle128B);
                     mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
@@ -286,13 +286,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int blk = 0; blk < 4; ++blk)            // latent columns: A from TMEM
                     for (int k = 0; k < 4; ++k) {
                         const uint64_t b = smem_desc(smem_u32(s.kv[st][blk]) + k * 32, 16, 1024, kLayoutSwizzle128B);
-                        mma_f16_ts(tmem_s[sb], tmem_q + blk * 32 + k * 8, b, idesc_s, (blk > 0 || k > 0) ? 1u : 0u);
+                        mma_f16_ts(tmem_s(sb), tmem_q + blk * 32 + k * 8, b, idesc_s, (blk > 0 || k > 0) ? 1u : 0u);
                     }
                 if (rank == 0)                                   // position columns: A from shared memory
                     for (int k = 0; k < 4; ++k) {
                         const uint64_t a = smem_desc(smem_u32(s.qp) + k * 32, 16, 1024, kLayoutSwizzle128B);
                         const uint64_t b = smem_desc(smem_u32(s.kv[st][4]) + k * 32, 16, 1024, kLayoutSwizzle128B);
-                        mma_f16_ss(tmem_s[sb], a, b, idesc_s, 1u);
+                        mma_f16_ss(tmem_s(sb), a, b, idesc_s, 1u);
                     }
                 mma_commit(&s.s_full[sb]);
                 if (kt > 0 && !issue_pv(kt - 1)) { ok = false; break; }
@@ -310,13 +310,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // peer's partial, softmax, P into TMEM.
         const int r = tid;
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        uint32_t recv_peer[2], recv_full_peer[2], can_send_peer[2];
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            recv_peer[b] = peer_addr(smem_u32(&s.recv[b][r * kN]), peer);
-            recv_full_peer[b] = peer_addr(smem_u32(&s.recv_full[b]), peer);
-            can_send_peer[b] = peer_addr(smem_u32(&s.can_send[b]), peer);
-        }
+        // peer addresses of receive buffer b (and its barriers): base + b * stride
+        const uint32_t recv_peer0 = peer_addr(smem_u32(&s.recv[0][r * kN]), peer);
+        const uint32_t recv_full_peer0 = peer_addr(smem_u32(&s.recv_full[0]), peer);
+        const uint32_t can_send_peer0 = peer_addr(smem_u32(&s.can_send[0]), peer);
+        auto recv_peer = [&](int b) { return recv_peer0 + (uint32_t)b * (uint32_t)sizeof(s.recv[0]); };
+        auto recv_full_peer = [&](int b) { return recv_full_peer0 + (uint32_t)b * 8u; };
+        auto can_send_peer = [&](int b) { return can_send_peer0 + (uint32_t)b * 8u; };
         const int sw = r & 15;                   // chunk swizzle of row r
         {
             // latent Q row (this CTA's 256 columns) into TMEM as 16-bit pairs; rows past H are zero
@@ -346,19 +346,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, mbar_wait(&s.s_full[t & 1], (t / 2) & 1))) return false;
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < kN; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem_s[t & 1] + lane_off + c, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) sc[c + i] = __uint_as_float(v[i]);
-            }
+            for (int c = 0; c < kN; c += 32) tmem_ld32f(tmem_s(t & 1) + lane_off + c, sc + c);
+            tmem_wait_ld();
             if (r == 0) mbar_arrive_expect_tx(&s.recv_full[b], kHeads * kN * 4);   // my receive of tile t
             if (t >= 2 && !__all_sync(0xffffffffu, wait_cluster(&s.can_send[b], ((t / 2) - 1) & 1))) return false;
 #pragma unroll
             for (int c = 0; c < kN / 4; ++c)
-                st_async_v4(recv_peer[b] + ((c ^ sw) * 16), sc[4 * c], sc[4 * c + 1], sc[4 * c + 2], sc[4 * c + 3],
-                            recv_full_peer[b]);
+                st_async_v4(recv_peer(b) + ((c ^ sw) * 16), sc[4 * c], sc[4 * c + 1], sc[4 * c + 2], sc[4 * c + 3],
+                            recv_full_peer(b));
             return true;
         };
         for (int kt = 0; ok && kt < n_kt; ++kt) {
@@ -371,21 +366,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, wait_cluster(&s.recv_full[sb], (kt / 2) & 1));
             if (!ok) break;
             const float *mine = &s.recv[sb][r * kN];
+            float2 *cur2 = reinterpret_cast<float2 *>(cur);
 #pragma unroll
             for (int c = 0; c < kN / 4; ++c) {
                 const float4 o = *reinterpret_cast<const float4 *>(mine + ((c ^ sw) * 4));
-                cur[4 * c] += o.x; cur[4 * c + 1] += o.y; cur[4 * c + 2] += o.z; cur[4 * c + 3] += o.w;
+                cur2[2 * c] = fadd2(cur2[2 * c], make_float2(o.x, o.y));
+                cur2[2 * c + 1] = fadd2(cur2[2 * c + 1], make_float2(o.z, o.w));
             }
-            // online softmax (identical on both CTAs)
-            float mt = -INFINITY;
+            // online softmax (identical on both CTAs); keys past the visible range score -inf
+            if (valid < kN) {
 #pragma unroll
-            for (int c = 0; c < kN; ++c) {
-                cur[c] = c < valid ? cur[c] * prm.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, cur[c]);
+                for (int c = 0; c < kN; ++c)
+                    if (c >= valid) cur[c] = -INFINITY;
             }
+            float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kN; c += 4) {
+                ma = fmax3(ma, cur[c], cur[c + 1]);
+                mb = fmax3(mb, cur[c + 2], cur[c + 3]);
+            }
+            const float mt = fmaxf(ma, mb) * prm.scale_log2;   // the scale is positive
             // this warp's rows of recv[sb] are read (mt depends on every loaded value)
             const float wdep = __shfl_sync(0xffffffffu, mt, 0) + __shfl_sync(0xffffffffu, mt, 31);
-            if (lane == 0) arrive_remote_after(can_send_peer[sb], wdep);
+            if (lane == 0) arrive_remote_after(can_send_peer(sb), wdep);
             float alpha = 1.f;
             if (mt > m_ref + kSlack) {
                 alpha = exp2f(m_ref - mt);
@@ -407,22 +410,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
             }
-            // P = exp2(s - m_ref) as 16-bit pairs over this row's S columns (already read)
-            float lsum = 0.f;
+            // P = exp2(s * scale - m_ref) as 16-bit pairs over this row's S columns
+            // (already read); every tile has a visible key, so m_ref is finite here
+            const float2 sc2 = make_float2(prm.scale_log2, prm.scale_log2);
+            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            float2 ls2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < kN; c += 32) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = exp2f(cur[c + 2 * i] - m_ref);
-                    const float p1 = exp2f(cur[c + 2 * i + 1] - m_ref);
-                    lsum += p0 + p1;
-                    pk[i] = pack2<T>(p0, p1);
+                    const float2 x = ffma2(cur2[c / 2 + i], sc2, nm2);
+                    const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                    ls2 = fadd2(ls2, pp);
+                    pk[i] = pack2<T>(pp.x, pp.y);
                 }
-                tmem_st16(tmem_s[pb] + lane_off + c / 2, pk);
+                tmem_st16(tmem_s(pb) + lane_off + c / 2, pk);
             }
             tmem_wait_st();
-            l = l * alpha + lsum;
+            l = l * alpha + (ls2.x + ls2.y);
             // latent rows past the visible range must not reach P.V (tail slots may hold NaN)
             if (valid < kN) {
                 const int st = kt % kStages;

@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
-    const uint32_t tmem_s[3] = {tmem, tmem + 128, tmem + 256};   // S / P buffers
+    auto tmem_s = [tmem](int b) -> uint32_t { return tmem + 128u * (uint32_t)b; };   // S / P buffers 0..2
     const uint32_t tmem_o = tmem + 384;
 
     if (warp == 8) {
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int st = kt % kStages;
                 const uint32_t v_addr = smem_u32(s.v[st]);
-                const uint32_t p_tmem = tmem_s[kt % 3];          // P (16-bit pairs) over the S columns
+                const uint32_t p_tmem = tmem_s(kt % 3);          // P (16-bit pairs) over the S columns
                 for (int ks = 0; ks < kN / 16; ++ks) {
                     const uint64_t b = smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, kLayoutSwizzle128B);
                     mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t k_addr = smem_u32(s.k[st]);
                 for (int ks = 0; ks < kD / 16; ++ks) {
                     const uint32_t o = (ks / 4) * kHalfBytes + (ks % 4) * 32;
-                    mma_f16_ss(tmem_s[sb], smem_desc(q_addr + o, 16, 1024, kLayoutSwizzle128B),
+                    mma_f16_ss(tmem_s(sb), smem_desc(q_addr + o, 16, 1024, kLayoutSwizzle128B),
                                smem_desc(k_addr + o, 16, 1024, kLayoutSwizzle128B), idesc_s, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&s.s_full[sb]);
@@ -255,13 +255,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kbase = kt * kN + col0;
             // my 64 scores of the row into registers (two loads, one wait)
             uint32_t sv[64];
-            tmem_ld32(tmem_s[sb] + lane_off + col0, sv);
-            tmem_ld32(tmem_s[sb] + lane_off + col0 + 32, sv + 32);
+            tmem_ld32(tmem_s(sb) + lane_off + col0, sv);
+            tmem_ld32(tmem_s(sb) + lane_off + col0 + 32, sv + 32);
             tmem_wait_ld();
-            float mine = -INFINITY;
+            // keys at or past the row's visible end score -inf (diagonal and sequence-end tiles only)
+            if (kbase + 64 > vis_end) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-                if (kbase + c < vis_end) mine = fmaxf(mine, __uint_as_float(sv[c]) * prm.scale_log2);
+                for (int c = 0; c < 64; ++c)
+                    if (kbase + c >= vis_end) sv[c] = 0xff800000u;
+            }
+            // row maximum of the raw scores (the scale is positive, so it commutes with max)
+            float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+                ma = fmax3(ma, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+                mb = fmax3(mb, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+            }
+            const float mine = fmaxf(ma, mb) * prm.scale_log2;
             float other;
             ok = exchange(mine, other);
             if (!ok) break;
@@ -287,23 +297,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
             }
-            // P = exp2(s - m_ref) as 16-bit pairs over my S columns (already in registers)
-            float lsum = 0.f;
+            // P = exp2(s * scale - m_ref) as 16-bit pairs over my S columns (already in
+            // registers); masked keys hold -inf and give 0.  Every row sees key 0, so
+            // m_ref is finite from the first tile on.
+            const float2 sc2 = make_float2(prm.scale_log2, prm.scale_log2);
+            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            float2 ls2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < 64; c += 32) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int k0 = kbase + c + 2 * i;
-                    const float p0 = k0 < vis_end ? exp2f(__uint_as_float(sv[c + 2 * i]) * prm.scale_log2 - m_ref) : 0.f;
-                    const float p1 = k0 + 1 < vis_end ? exp2f(__uint_as_float(sv[c + 2 * i + 1]) * prm.scale_log2 - m_ref) : 0.f;
-                    lsum += p0 + p1;
-                    pk[i] = pack2<T>(p0, p1);
+                    const float2 x = ffma2(make_float2(__uint_as_float(sv[c + 2 * i]), __uint_as_float(sv[c + 2 * i + 1])),
+                                           sc2, nm2);
+                    const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                    ls2 = fadd2(ls2, pp);
+                    pk[i] = pack2<T>(pp.x, pp.y);
                 }
-                tmem_st16(tmem_s[sb] + lane_off + (col0 + c) / 2, pk);
+                tmem_st16(tmem_s(sb) + lane_off + (col0 + c) / 2, pk);
             }
             tmem_wait_st();
-            l = l * alpha + lsum;
+            l = l * alpha + (ls2.x + ls2.y);
             // V rows at or past the sequence end (tail slots) must not reach the MMA
             if (kt * kN + kN > seq_len) {
                 const int st = kt % kStages;
