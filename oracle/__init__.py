@@ -62,14 +62,14 @@ def _lib(plant: int = 0) -> ctypes.CDLL:
     if plant not in _LIBS:
         lib = ctypes.CDLL(build(plant))
         prob = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64, _i64, _i64, _i64, _i64,
-                _vp, _i64, _vp, _i64, _vp, _vp, _i64, _i64, ctypes.c_double, ctypes.c_int]
+                _vp, _i64, _vp, _i64, _vp, _vp, _i64, _i64, ctypes.c_double, ctypes.c_int, _i64]
         lib.pa_oracle_attention.argtypes = prob + [_vp, _i64, _vp, _vp, ctypes.c_int]
         lib.pa_oracle_attention.restype = ctypes.c_int
         lib.pa_oracle_attention_split.argtypes = prob + [_vp, _i64, _i64, _vp, _vp, ctypes.c_int]
         lib.pa_oracle_attention_split.restype = ctypes.c_int
         lib.pa_oracle_merge.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _vp]
         lib.pa_oracle_merge.restype = None
-        lib.pa_oracle_split_range.argtypes = [_i64, _i64, _i64, _i64,
+        lib.pa_oracle_split_range.argtypes = [_i64, _i64, _i64, _i64, _i64,
                                               ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
         lib.pa_oracle_kv_store.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                            _vp, _i64, _vp, _vp, _i64]
@@ -105,7 +105,7 @@ def _ptr(t):
 
 
 def _problem(q, k_cache, v_cache, seq_lens, block_table, query_seq, query_pos, scale, causal,
-             qp=None, kp_cache=None):
+             qp=None, kp_cache=None, window=0):
     """Marshal tensors to the C problem arguments. Returns (args, keepalive, hq, dv)."""
     q, k_cache, v_cache, qp, kp_cache = (_cpu(t) for t in (q, k_cache, v_cache, qp, kp_cache))
     if q.dtype not in _DTYPE_CODE:
@@ -128,7 +128,7 @@ def _problem(q, k_cache, v_cache, seq_lens, block_table, query_seq, query_pos, s
     args = [_ptr(q), _ptr(qp), _ptr(k_cache), _ptr(v_cache), _ptr(kp_cache), _DTYPE_CODE[q.dtype],
             nq, hq, hkv, d, dv, p, _ptr(seq_lens), len(seq_lens), _ptr(block_table),
             block_table.shape[1], _ptr(query_seq), _ptr(query_pos), ps, pages, float(scale),
-            1 if causal else 0]
+            1 if causal else 0, int(window)]
     keep = (q, k_cache, v_cache, qp, kp_cache, seq_lens, block_table, query_seq, query_pos)
     return args, keep, nq, hq, dv
 
@@ -143,15 +143,16 @@ def _rows_arg(rows, nq, hq):
 
 
 def attention(q, k_cache, v_cache, seq_lens, block_table, query_seq, query_pos, scale,
-              causal=True, qp=None, kp_cache=None, rows=None, nthreads=0, plant=0):
+              causal=True, qp=None, kp_cache=None, rows=None, nthreads=0, plant=0, window=0):
     """fp64 paged attention.
 
     Returns (out, lse): out is float64 [Q, Hq, Dv] when rows is None, else
     [len(rows), Dv] for the flat (q * Hq + h) indices in ``rows``.  For MLA pass
-    the latent cache as both k_cache and v_cache plus qp / kp_cache.
+    the latent cache as both k_cache and v_cache plus qp / kp_cache.  window > 0
+    limits a query at position p to keys p - window + 1 and later.
     """
     args, keep, nq, hq, dv = _problem(q, k_cache, v_cache, seq_lens, block_table, query_seq,
-                                      query_pos, scale, causal, qp, kp_cache)
+                                      query_pos, scale, causal, qp, kp_cache, window)
     r, nrows = _rows_arg(rows, nq, hq)
     out = np.zeros((nrows, dv), dtype=np.float64)
     lse = np.zeros((nrows,), dtype=np.float64)
@@ -165,10 +166,11 @@ def attention(q, k_cache, v_cache, seq_lens, block_table, query_seq, query_pos, 
 
 
 def attention_split(q, k_cache, v_cache, seq_lens, block_table, query_seq, query_pos, scale,
-                    splits, causal=True, qp=None, kp_cache=None, rows=None, nthreads=0, plant=0):
+                    splits, causal=True, qp=None, kp_cache=None, rows=None, nthreads=0, plant=0,
+                    window=0):
     """Per-split partials: (out_part [S, rows, Dv], lse_part [S, rows]) in fp64."""
     args, keep, nq, hq, dv = _problem(q, k_cache, v_cache, seq_lens, block_table, query_seq,
-                                      query_pos, scale, causal, qp, kp_cache)
+                                      query_pos, scale, causal, qp, kp_cache, window)
     r, nrows = _rows_arg(rows, nq, hq)
     out = np.zeros((splits, nrows, dv), dtype=np.float64)
     lse = np.zeros((splits, nrows), dtype=np.float64)
@@ -191,10 +193,10 @@ def merge(out_part, lse_part):
     return out, lse
 
 
-def split_range(n, splits, s, page_size):
-    """[j0, j1) of split s of n visible keys, as the oracle partitions them."""
+def split_range(n, splits, s, page_size, lo=0):
+    """[j0, j1) of split s of the visible keys [lo, n), as the oracle partitions them."""
     a, b = _i64(), _i64()
-    _lib().pa_oracle_split_range(int(n), int(splits), int(s), int(page_size),
+    _lib().pa_oracle_split_range(int(lo), int(n), int(splits), int(s), int(page_size),
                                  ctypes.byref(a), ctypes.byref(b))
     return a.value, b.value
 

@@ -27,6 +27,9 @@
  *    is the reference result.
  *  - same page, `append_with_report`: new rows [queries, heads, d|dv] are
  *    written into the caches at the plan's positions.
+ *  - libmir-cuda 0.1.0, src/backend/attention/graph/mod.rs, `Geometry`: a
+ *    layer's attention carries a `window` next to its head geometry, and the
+ *    split configuration is chosen from the token count and that window.
  *  - boostr 0.1.0, src/inference/decode_graph.rs, `DeviceScalars::update`: a
  *    decode step writes its key/value at position seq_len and then attends
  *    over seq_len + 1 keys, i.e. the query at absolute position p sees keys
@@ -40,7 +43,15 @@
  *  - split partition: n visible keys, chunk = ceil(n / S) rounded up to a
  *    multiple of page_size, split s covers [s*chunk, min((s+1)*chunk, n));
  *    an empty split has lse = -inf and a zero partial output;
- *  - lse is the natural-log log-sum-exp of the scaled scores.
+ *  - lse is the natural-log log-sum-exp of the scaled scores;
+ *  - sliding window W > 0 (the pages name the field but not its meaning): a
+ *    query at position p sees only keys j >= p - W + 1, on top of the causal
+ *    or non-causal upper end; W = 0 means no window;
+ *  - split partition under a window: the visible keys are [lo, hi); with
+ *    base = lo rounded down to a page boundary and chunk = ceil((hi - base) / S)
+ *    rounded up to a multiple of page_size, split s covers
+ *    [max(lo, base + s*chunk), min(base + (s+1)*chunk, hi)) (W = 0 gives the
+ *    rule above, since lo = base = 0).
  *
  * All arithmetic is IEEE binary64 in plain loops, one (query, head) row per
  * OpenMP iteration, in key order.  Inputs are read in their storage type
@@ -51,6 +62,7 @@
  *   1 causal range drops the query's own key   2 scale applied twice
  *   3 GQA head map h % Hkv instead of h / G    4 MLA position term dropped
  *   5 page row taken as j / ps instead of j % ps
+ *   6 window lower end off by one (p - W instead of p - W + 1)
  */
 #include <math.h>
 #include <stdint.h>
@@ -107,9 +119,10 @@ typedef struct {
     int64_t page_size, pages;
     double scale;
     int causal;
+    int64_t window;
 } problem;
 
-/* Number of keys that query q may see. */
+/* Upper end (exclusive) of the keys that query q may see. */
 static int64_t visible(const problem *pb, int64_t q) {
     int64_t s = pb->qseq[q];
     if (pb->causal) {
@@ -120,6 +133,17 @@ static int64_t visible(const problem *pb, int64_t q) {
 #endif
     }
     return pb->seq_lens[s];
+}
+
+/* Lower end (inclusive) of the keys that query q may see. */
+static int64_t visible_from(const problem *pb, int64_t q) {
+    if (pb->window <= 0) return 0;
+#if PLANT == 6
+    int64_t lo = (int64_t)pb->qpos[q] - pb->window;
+#else
+    int64_t lo = (int64_t)pb->qpos[q] - pb->window + 1;
+#endif
+    return lo > 0 ? lo : 0;
 }
 
 /* Physical cache row (page * page_size + row-in-page) of logical key j. */
@@ -195,13 +219,19 @@ static void attend_range(const problem *pb, int64_t q, int64_t h, int64_t j0, in
     *lse = m + log(sum);
 }
 
-/* Split s of S over n visible keys (see header for the reading). */
-static void split_range(int64_t n, int64_t splits, int64_t s, int64_t ps, int64_t *j0, int64_t *j1) {
+/* Split s of S over the visible keys [lo, hi) (see header for the reading). */
+static void split_range(int64_t lo, int64_t hi, int64_t splits, int64_t s, int64_t ps, int64_t *j0,
+                        int64_t *j1) {
+    int64_t base = (lo / ps) * ps;
+    int64_t n = hi - base;
+    if (n < 0) n = 0;
     int64_t chunk = (n + splits - 1) / splits;
     chunk = ((chunk + ps - 1) / ps) * ps;
-    int64_t b = s * chunk, e = b + chunk;
-    if (b > n) b = n;
-    if (e > n) e = n;
+    int64_t b = base + s * chunk, e = b + chunk;
+    if (b < lo) b = lo;
+    if (b > hi) b = hi;
+    if (e > hi) e = hi;
+    if (e < b) e = b;
     *j0 = b;
     *j1 = e;
 }
@@ -221,11 +251,11 @@ static int64_t max_visible(const problem *pb, const int64_t *rows, int64_t nrows
     int dtype, int64_t queries, int64_t hq, int64_t hkv, int64_t d, int64_t dv,          \
     int64_t p, const int32_t *seq_lens, int64_t seqs, const int32_t *table,              \
     int64_t width, const int32_t *qseq, const int32_t *qpos, int64_t page_size,          \
-    int64_t pages, double scale, int causal
+    int64_t pages, double scale, int causal, int64_t window
 
 #define PROBLEM_INIT                                                                     \
     problem pb = {q, qp, k, v, kp, dtype, queries, hq, hkv, d, dv, p, seq_lens, seqs,    \
-                  table, width, qseq, qpos, page_size, pages, scale, causal}
+                  table, width, qseq, qpos, page_size, pages, scale, causal, window}
 
 /*
  * Unsplit attention.  rows: NULL for every (query, head) in order, else a
@@ -254,7 +284,7 @@ int pa_oracle_attention(PROBLEM_ARGS, const int64_t *rows, int64_t nrows,
             if (!scores) continue;
             int64_t flat = rows ? rows[i] : i;
             int64_t qi = flat / hq, h = flat % hq;
-            attend_range(&pb, qi, h, 0, visible(&pb, qi), scores, out + i * dv, lse + i);
+            attend_range(&pb, qi, h, visible_from(&pb, qi), visible(&pb, qi), scores, out + i * dv, lse + i);
         }
         free(scores);
     }
@@ -288,10 +318,10 @@ int pa_oracle_attention_split(PROBLEM_ARGS, const int64_t *rows, int64_t nrows, 
             if (!scores) continue;
             int64_t flat = rows ? rows[i] : i;
             int64_t qi = flat / hq, h = flat % hq;
-            int64_t n = visible(&pb, qi);
+            int64_t lo = visible_from(&pb, qi), hi = visible(&pb, qi);
             for (int64_t sp = 0; sp < splits; ++sp) {
                 int64_t j0, j1;
-                split_range(n, splits, sp, page_size, &j0, &j1);
+                split_range(lo, hi, splits, sp, page_size, &j0, &j1);
                 attend_range(&pb, qi, h, j0, j1, scores, out_part + (sp * nrows + i) * dv,
                              lse_part + sp * nrows + i);
             }
@@ -328,8 +358,9 @@ void pa_oracle_merge(const double *out_part, const double *lse_part, int64_t spl
 }
 
 /* Split bounds as the oracle partitions them (exposed for the tests). */
-void pa_oracle_split_range(int64_t n, int64_t splits, int64_t s, int64_t ps, int64_t *j0, int64_t *j1) {
-    split_range(n, splits, s, ps, j0, j1);
+void pa_oracle_split_range(int64_t lo, int64_t hi, int64_t splits, int64_t s, int64_t ps, int64_t *j0,
+                           int64_t *j1) {
+    split_range(lo, hi, splits, s, ps, j0, j1);
 }
 
 /*

@@ -14,6 +14,11 @@ append in `append_with_report`; boostr 0.1.0, src/inference/decode_graph.rs,
   * one visible key -> the value row exactly; equal scores -> mean of V;
   * log-sum-exp against scipy.special.logsumexp;
   * a naive pure-Python loop on tiny inputs;
+  * the sliding window (a layer's `window`, libmir-cuda 0.1.0,
+    src/backend/attention/graph/mod.rs, `Geometry`; read as: a query at
+    position p sees keys p - W + 1 and later) against SDPA with a band mask,
+    its two limits (W = 1: the own key's value row; W > p: no window), split
+    invariance and brute force;
   * closed-form worked examples in tests/golden/closed_forms.json;
   * the append as a page-level round trip.
 
@@ -64,8 +69,9 @@ def random_layout(seed, seq_lens, page_size, extra_pages=3):
     return table, pool
 
 
-def sdpa_reference(q, k_seq, v_seq, query_seq, query_pos, scale, causal, hkv):
-    """float64 SDPA per query on contiguous data; GQA by repeat_interleave."""
+def sdpa_reference(q, k_seq, v_seq, query_seq, query_pos, scale, causal, hkv, window=0):
+    """float64 SDPA per query on contiguous data; GQA by repeat_interleave;
+    window > 0 adds a band mask (keys j >= pos - window + 1)."""
     nq, hq, _ = q.shape
     outs = []
     for i in range(nq):
@@ -76,6 +82,8 @@ def sdpa_reference(q, k_seq, v_seq, query_seq, query_pos, scale, causal, hkv):
         mask = torch.ones(1, n, dtype=torch.bool)
         if causal:
             mask = (torch.arange(n) <= pos).view(1, n)
+        if window > 0:
+            mask = mask & (torch.arange(n) >= pos - window + 1).view(1, n)
         o = F.scaled_dot_product_attention(
             q[i].double().unsqueeze(1),            # [Hq, 1, D]
             k.transpose(0, 1), v.transpose(0, 1),  # [Hq, n, D]
@@ -206,7 +214,7 @@ def pin_logsumexp(plant=0):
             np.testing.assert_allclose(lse[i, h], logsumexp(sc), rtol=1e-13, atol=1e-13)
 
 
-def naive_python(q, k_seq, v_seq, qseq, qpos, scale, causal):
+def naive_python(q, k_seq, v_seq, qseq, qpos, scale, causal, window=0):
     nq, hq, d = len(q), len(q[0]), len(q[0][0])
     out = []
     for i in range(nq):
@@ -216,11 +224,13 @@ def naive_python(q, k_seq, v_seq, qseq, qpos, scale, causal):
             hkv = len(kk[0])
             g = hq // hkv
             n = qpos[i] + 1 if causal else len(kk)
-            sc = [scale * sum(q[i][h][e] * kk[j][h // g][e] for e in range(d)) for j in range(n)]
+            first = max(0, qpos[i] - window + 1) if window > 0 else 0
+            keys = list(range(first, n))
+            sc = [scale * sum(q[i][h][e] * kk[j][h // g][e] for e in range(d)) for j in keys]
             m = max(sc)
             w = [math.exp(x - m) for x in sc]
             tot = sum(w)
-            rows.append([sum(w[j] * vv[j][h // g][e] for j in range(n)) / tot
+            rows.append([sum(w[t] * vv[j][h // g][e] for t, j in enumerate(keys)) / tot
                          for e in range(len(vv[0][0]))])
         out.append(rows)
     return np.array(out)
@@ -238,6 +248,51 @@ def pin_brute_force(plant=0):
         ref = naive_python(pr["q"].double().tolist(), [k.double().tolist() for k in pr["k_seq"]],
                            [v.double().tolist() for v in pr["v_seq"]], pr["qseq"].tolist(),
                            pr["qpos"].tolist(), 0.7, causal)
+        np.testing.assert_allclose(out, ref, rtol=1e-14, atol=1e-14)
+
+
+def pin_window(plant=0):
+    """Sliding window: SDPA with a band mask, the limits W = 1 and W > p,
+    split invariance under the window, and brute force."""
+    seq_lens = [1, 9, 33, 70]
+    queries = decode_queries(seq_lens) + [(3, 40), (2, 5), (3, 0), (1, 3)]
+    for (hq, hkv, causal, dtype, ps) in [(4, 2, True, torch.float32, 8), (6, 3, False, torch.bfloat16, 4)]:
+        pr = contiguous_problem(91 + hq, seq_lens, queries, hq, hkv, 16, 12, ps, dtype, causal)
+        kc = paged_from_contiguous(pr["k_seq"], pr["table"], ps, pr["pool"])
+        vc = paged_from_contiguous(pr["v_seq"], pr["table"], ps, pr["pool"])
+        args = (pr["q"], kc, vc, pr["seq_lens"], pr["table"], pr["qseq"], pr["qpos"], 0.41)
+        for w in (1, 2, 5, 17, 64):
+            out, lse = oracle.attention(*args, causal=causal, window=w, plant=plant)
+            ref = sdpa_reference(pr["q"], pr["k_seq"], pr["v_seq"], pr["qseq"], pr["qpos"], 0.41, causal, hkv,
+                                 window=w)
+            np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+            for sp in (2, 3, 8):
+                op, lp = oracle.attention_split(*args, splits=sp, causal=causal, window=w, plant=plant)
+                mo, ml = oracle.merge(op, lp)
+                np.testing.assert_allclose(mo.reshape(out.shape), out, rtol=1e-12, atol=1e-12)
+                np.testing.assert_allclose(ml.reshape(lse.shape), lse, rtol=1e-12, atol=1e-12)
+        if causal:
+            # W = 1: each query sees only its own key
+            out, _ = oracle.attention(*args, causal=True, window=1, plant=plant)
+            for i, (sq, pos) in enumerate(queries):
+                v = pr["v_seq"][sq][pos].double().repeat_interleave(hq // hkv, dim=0).numpy()
+                assert np.array_equal(out[i], v)
+        # a window longer than every position is no window, bit for bit
+        o0, l0 = oracle.attention(*args, causal=causal, plant=plant)
+        o1, l1 = oracle.attention(*args, causal=causal, window=1000, plant=plant)
+        assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    # brute force on a tiny case
+    seq_lens = [3, 8, 6]
+    queries = [(0, 2), (1, 7), (1, 4), (2, 5), (2, 0)]
+    pr = contiguous_problem(97, seq_lens, queries, 4, 2, 4, 3, 2, torch.float32, True)
+    kc = paged_from_contiguous(pr["k_seq"], pr["table"], 2, pr["pool"])
+    vc = paged_from_contiguous(pr["v_seq"], pr["table"], 2, pr["pool"])
+    for w in (2, 3):
+        out, _ = oracle.attention(pr["q"], kc, vc, pr["seq_lens"], pr["table"], pr["qseq"], pr["qpos"],
+                                  0.7, causal=True, window=w, plant=plant)
+        ref = naive_python(pr["q"].double().tolist(), [k.double().tolist() for k in pr["k_seq"]],
+                           [v.double().tolist() for v in pr["v_seq"]], pr["qseq"].tolist(),
+                           pr["qpos"].tolist(), 0.7, True, window=w)
         np.testing.assert_allclose(out, ref, rtol=1e-14, atol=1e-14)
 
 
@@ -289,7 +344,7 @@ def pin_store_round_trip(plant=0):
 
 PINS = [pin_sdpa_mha_gqa, pin_sdpa_mla, pin_permutation_invariance, pin_split_invariance,
         pin_single_key, pin_equal_scores, pin_logsumexp, pin_brute_force, pin_golden,
-        pin_store_round_trip]
+        pin_store_round_trip, pin_window]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -308,6 +363,16 @@ def test_split_range_partition():
                 assert (b - a) % 16 == 0 or b == n
                 prev = b
             assert prev == n
+    # under a window the visible keys start at lo; later split starts fall on page boundaries
+    for lo, n in ((5, 40), (37, 100), (64, 65), (1000, 131072)):
+        for s_count in (1, 2, 5, 64):
+            prev = lo
+            for s in range(s_count):
+                a, b = oracle.split_range(n, s_count, s, 16, lo=lo)
+                assert a == prev and b >= a
+                assert a == lo or a % 16 == 0 or a == n
+                prev = b
+            assert prev == n
 
 
 def test_workload_shapes():
@@ -324,7 +389,7 @@ def test_workload_shapes():
     assert not torch.isnan(c.k_cache[int(c.block_table[0, 0]), 0].float()).any()
 
 
-@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6])
 def test_planted_mistakes_are_caught(plant):
     """Each deliberately broken oracle build must fail at least one pin."""
     failures = 0
