@@ -59,7 +59,7 @@ typedef enum {
 
 typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
 
-#define PA_ABI_VERSION 1
+#define PA_ABI_VERSION 2
 #define PA_MAX_SPLITS 64                        /* `MAX_SPLITS` of the split workspace      */
 #define PA_MAX_HEAD_DIM 1024                    /* d, dv <= 1024 (`execute_attention_into`) */
 #define PA_MAX_POS_DIM 256                      /* MLA position dim P <= 256                */
@@ -145,18 +145,20 @@ size_t pa_workspace_bytes(int32_t queries, int32_t heads, int32_t value_dim, int
  * (libmir-cuda 0.1.0, src/backend/attention/graph/mod.rs enables a split
  * path above a `split_threshold`; its value is not given, this rule is ours):
  * enough (item, kv head, split) blocks to give every SM about four, no split
- * shorter than 4 pages of the longest visible history, 1..PA_MAX_SPLITS.
+ * shorter than 4 pages of the longest visible history (at most `window` keys
+ * when window > 0), 1..PA_MAX_SPLITS.
  */
 int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t num_kv_heads,
-                                   int32_t num_sms);
+                                   int32_t window, int32_t num_sms);
 
 /*
  * Split count for paged_mla_forward (same source as above; the rule is ours):
  * the tensor-core MLA kernel runs one CTA pair per (query, 128 heads, split);
  * aim for about two waves over `num_sms` SMs, each split keeping at least 256
- * keys of the longest history, 1..PA_MAX_SPLITS.
+ * keys of the longest history (at most `window` keys when window > 0),
+ * 1..PA_MAX_SPLITS.
  */
-int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t num_sms);
+int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t window, int32_t num_sms);
 
 /*
  * One decode step forward, on the device: every query of an uploaded plan
@@ -200,7 +202,11 @@ pa_status paged_kv_store(const pa_plan *plan, const void *new_k, const void *new
  * for query q and head h, with kv = h / (num_heads / num_kv_heads),
  *   out[q, h, :] = sum_j softmax_j(scale * q[q,h,:] . K_j) V_j
  * over the keys j that q sees (causal: 0..pos; else 0..seq_len-1), K_j / V_j
- * gathered through the block table from head kv.
+ * gathered through the block table from head kv.  window > 0 is a sliding
+ * window: the keys start at pos - window + 1 (a layer's `window`, libmir-cuda
+ * 0.1.0, src/backend/attention/graph/mod.rs, `Geometry`; the pages name the
+ * field only, this reading is ours); window == 0 is no window; < 0 is
+ * PA_ERR_ARG.
  *
  *   q       [queries, num_heads, head_dim]
  *   k_cache [pages, page_size, num_kv_heads, head_dim]
@@ -213,13 +219,15 @@ pa_status paged_kv_store(const pa_plan *plan, const void *new_k, const void *new
 pa_status paged_attn_forward(const pa_plan *plan, const void *q, const void *k_cache,
                              const void *v_cache, void *out, int32_t num_heads,
                              int32_t num_kv_heads, int32_t head_dim, int32_t value_dim,
-                             float scale, int32_t causal, pa_dtype dtype, pa_stream_t stream);
+                             float scale, int32_t causal, int32_t window, pa_dtype dtype,
+                             pa_stream_t stream);
 
 /*
- * Split-KV form (`attention_into_split`): the visible history of every decode
- * query is cut into `splits` contiguous ranges (n visible keys, chunk =
- * ceil(n / splits) rounded up to a multiple of page_size, split s covers
- * [s*chunk, min((s+1)*chunk, n))); each range writes its normalised fp32
+ * Split-KV form (`attention_into_split`): the visible history [lo, hi) of
+ * every decode query is cut into `splits` contiguous ranges (base = lo rounded
+ * down to a page boundary, chunk = ceil((hi - base) / splits) rounded up to a
+ * multiple of page_size, split s covers [max(lo, base + s*chunk),
+ * min(base + (s+1)*chunk, hi)); lo = 0 without a window); each range writes its normalised fp32
  * partial output and natural-log log-sum-exp into `workspace`, then a merge
  * kernel writes out.  Prefill tiles are computed unsplit.  The workspace
  * (>= pa_workspace_bytes(queries, num_heads, value_dim, splits), 16-byte
@@ -230,8 +238,9 @@ pa_status paged_attn_forward(const pa_plan *plan, const void *q, const void *k_c
 pa_status paged_attn_forward_split(const pa_plan *plan, const void *q, const void *k_cache,
                                    const void *v_cache, void *out, int32_t num_heads,
                                    int32_t num_kv_heads, int32_t head_dim, int32_t value_dim,
-                                   float scale, int32_t causal, pa_dtype dtype, void *workspace,
-                                   size_t workspace_bytes, int32_t splits, pa_stream_t stream);
+                                   float scale, int32_t causal, int32_t window, pa_dtype dtype,
+                                   void *workspace, size_t workspace_bytes, int32_t splits,
+                                   pa_stream_t stream);
 
 /*
  * MLA attention (`DevicePlan::mla`, `mla_with_workspace`): one shared latent
@@ -247,12 +256,12 @@ pa_status paged_attn_forward_split(const pa_plan *plan, const void *q, const voi
  * `scale` comes from the model's original QK head dims, not the latent rank.
  * 1 <= latent_dim <= 1024, 1 <= pos_dim <= 256.  workspace may be NULL (then
  * splits must be 1); otherwise the split rules of paged_attn_forward_split
- * apply with value_dim = latent_dim.
+ * apply with value_dim = latent_dim.  `window` as for paged_attn_forward.
  */
 pa_status paged_mla_forward(const pa_plan *plan, const void *q, const void *qp,
                             const void *latent_cache, const void *pos_cache, void *out,
                             int32_t num_heads, int32_t latent_dim, int32_t pos_dim, float scale,
-                            int32_t causal, pa_dtype dtype, void *workspace,
+                            int32_t causal, int32_t window, pa_dtype dtype, void *workspace,
                             size_t workspace_bytes, int32_t splits, pa_stream_t stream);
 
 /*
@@ -279,8 +288,8 @@ pa_status paged_mla_forward(const pa_plan *plan, const void *q, const void *qp,
 pa_status paged_attn_forward_split_static(const pa_plan *plan, const void *q, const void *k_cache,
                                           const void *v_cache, void *out, int32_t num_heads,
                                           int32_t num_kv_heads, int32_t head_dim, int32_t value_dim,
-                                          float scale, int32_t causal, pa_dtype dtype, int32_t splits,
-                                          pa_stream_t stream);
+                                          float scale, int32_t causal, int32_t window, pa_dtype dtype,
+                                          int32_t splits, pa_stream_t stream);
 
 /*
  * Profiling hook: the next attention call made on this thread records

@@ -73,19 +73,19 @@ def load() -> ctypes.CDLL:
     lib.pa_plan_describe.restype = ctypes.c_int
     lib.pa_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.pa_workspace_bytes.restype = sz
-    lib.paged_attn_split_heuristic.argtypes = [vp, i32, i32, i32]
+    lib.paged_attn_split_heuristic.argtypes = [vp, i32, i32, i32, i32]
     lib.paged_attn_split_heuristic.restype = i32
-    lib.paged_mla_split_heuristic.argtypes = [vp, i32, i32]
+    lib.paged_mla_split_heuristic.argtypes = [vp, i32, i32, i32]
     lib.paged_mla_split_heuristic.restype = i32
     lib.paged_kv_store.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int, vp]
     lib.paged_kv_store.restype = ctypes.c_int
-    lib.paged_attn_forward.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, i32,
+    lib.paged_attn_forward.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, i32, i32,
                                        ctypes.c_int, vp]
     lib.paged_attn_forward.restype = ctypes.c_int
     lib.paged_attn_forward_split.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, i32,
-                                             ctypes.c_int, vp, sz, i32, vp]
+                                             i32, ctypes.c_int, vp, sz, i32, vp]
     lib.paged_attn_forward_split.restype = ctypes.c_int
-    lib.paged_mla_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_float, i32,
+    lib.paged_mla_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_float, i32, i32,
                                       ctypes.c_int, vp, sz, i32, vp]
     lib.paged_mla_forward.restype = ctypes.c_int
     lib.pa_plan_advance.argtypes = [vp, vp]
@@ -222,16 +222,18 @@ def make_workspace(plan: Plan, heads: int, value_dim: int, splits: int, device=N
     return torch.empty((n + 3) // 4, dtype=torch.float32, device=device or plan.device)
 
 
-def paged_attn_split_heuristic(plan: Plan, num_heads: int, num_kv_heads: int, num_sms: int | None = None) -> int:
+def paged_attn_split_heuristic(plan: Plan, num_heads: int, num_kv_heads: int, num_sms: int | None = None,
+                               window: int = 0) -> int:
     if num_sms is None:
         num_sms = torch.cuda.get_device_properties(plan.device or 0).multi_processor_count
-    return int(load().paged_attn_split_heuristic(plan.handle, int(num_heads), int(num_kv_heads), int(num_sms)))
+    return int(load().paged_attn_split_heuristic(plan.handle, int(num_heads), int(num_kv_heads), int(window),
+                                                 int(num_sms)))
 
 
-def paged_mla_split_heuristic(plan: Plan, num_heads: int, num_sms: int | None = None) -> int:
+def paged_mla_split_heuristic(plan: Plan, num_heads: int, num_sms: int | None = None, window: int = 0) -> int:
     if num_sms is None:
         num_sms = torch.cuda.get_device_properties(plan.device or 0).multi_processor_count
-    return int(load().paged_mla_split_heuristic(plan.handle, int(num_heads), int(num_sms)))
+    return int(load().paged_mla_split_heuristic(plan.handle, int(num_heads), int(window), int(num_sms)))
 
 
 def paged_kv_store(plan: Plan, new_k, new_v, k_cache, v_cache) -> None:
@@ -275,18 +277,20 @@ def _attn_common(plan, q, k_cache, v_cache, out):
     return out
 
 
-def paged_attn_forward(plan: Plan, q, k_cache, v_cache, scale: float, causal: bool = True, out=None):
-    """Paged MHA/GQA attention; returns out [queries, num_heads, value_dim]."""
+def paged_attn_forward(plan: Plan, q, k_cache, v_cache, scale: float, causal: bool = True, out=None,
+                       window: int = 0):
+    """Paged MHA/GQA attention; returns out [queries, num_heads, value_dim].
+    window > 0: a query at position p sees keys p - window + 1 and later."""
     out = _attn_common(plan, q, k_cache, v_cache, out)
     _check(load().paged_attn_forward(plan.handle, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                      out.data_ptr(), q.shape[1], k_cache.shape[2], q.shape[2],
-                                     v_cache.shape[3], float(scale), 1 if causal else 0, _DTYPES[q.dtype],
-                                     _stream(q.device)))
+                                     v_cache.shape[3], float(scale), 1 if causal else 0, int(window),
+                                     _DTYPES[q.dtype], _stream(q.device)))
     return out
 
 
 def paged_attn_forward_split(plan: Plan, q, k_cache, v_cache, scale: float, splits: int, workspace=None,
-                             causal: bool = True, out=None):
+                             causal: bool = True, out=None, window: int = 0):
     """Split-KV paged attention with an fp32 workspace (allocated here when not given)."""
     out = _attn_common(plan, q, k_cache, v_cache, out)
     if workspace is None:
@@ -294,7 +298,7 @@ def paged_attn_forward_split(plan: Plan, q, k_cache, v_cache, scale: float, spli
     _check_disjoint(out, workspace)
     _check(load().paged_attn_forward_split(plan.handle, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                            out.data_ptr(), q.shape[1], k_cache.shape[2], q.shape[2],
-                                           v_cache.shape[3], float(scale), 1 if causal else 0,
+                                           v_cache.shape[3], float(scale), 1 if causal else 0, int(window),
                                            _DTYPES[q.dtype], workspace.data_ptr(),
                                            workspace.numel() * workspace.element_size(), int(splits),
                                            _stream(q.device)))
@@ -302,7 +306,7 @@ def paged_attn_forward_split(plan: Plan, q, k_cache, v_cache, scale: float, spli
 
 
 def paged_mla_forward(plan: Plan, q, qp, latent_cache, pos_cache, scale: float, causal: bool = True,
-                      workspace=None, splits: int = 1, out=None):
+                      workspace=None, splits: int = 1, out=None, window: int = 0):
     """MLA attention over a shared latent head plus a rotated position cache."""
     dev, dt = q.device, q.dtype
     if dt not in _DTYPES:
@@ -334,7 +338,7 @@ def paged_mla_forward(plan: Plan, q, qp, latent_cache, pos_cache, scale: float, 
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().paged_mla_forward(plan.handle, q.data_ptr(), qp.data_ptr(), latent_cache.data_ptr(),
                                     pos_cache.data_ptr(), out.data_ptr(), q.shape[1], q.shape[2], qp.shape[2],
-                                    float(scale), 1 if causal else 0, _DTYPES[dt], ws_ptr, ws_bytes,
+                                    float(scale), 1 if causal else 0, int(window), _DTYPES[dt], ws_ptr, ws_bytes,
                                     int(splits), _stream(dev)))
     return out
 

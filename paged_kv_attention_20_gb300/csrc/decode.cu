@@ -37,14 +37,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;  // log2 units
 
-// Split s of n visible keys: chunk = ceil(n / S) rounded up to a page multiple.
-__device__ __forceinline__ void split_bounds(int64_t n, int splits, int s, int ps, int64_t &j0, int64_t &j1) {
-    int64_t chunk = (n + splits - 1) / splits;
-    chunk = (chunk + ps - 1) / ps * ps;
-    int64_t b = (int64_t)s * chunk, e = b + chunk;
-    j0 = b < n ? b : n;
-    j1 = e < n ? e : n;
-}
 
 template <typename T> __device__ __forceinline__ float to_f(T x);
 template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
@@ -156,12 +148,13 @@ __global__ void __launch_bounds__(128) decode_fast_kernel(AttnArgs a, int use_li
     const int4 meta = a.plan.qmeta[qi];
     const int seq = meta.x, pos = meta.y;
     const int ps = a.plan.page_size;
-    const int64_t n = a.causal ? (int64_t)pos + 1 : (int64_t)a.plan.seq_lens[seq];
+    int64_t lo, hi;
+    visible_range(pos, a.plan.seq_lens[seq], a.causal, a.window, lo, hi);
     const int kvh = blockIdx.y / groups;
     const int h0 = kvh * (a.hq / a.hkv) + (blockIdx.y % groups) * GH;
     const int split = blockIdx.z;
     int64_t j0, j1;
-    split_bounds(n, a.splits, split, ps, j0, j1);
+    split_bounds(lo, hi, a.splits, split, ps, j0, j1);
     const int ntiles = (int)((j1 - j0 + C::TK - 1) / C::TK);
     const int32_t *trow = a.plan.table + (int64_t)seq * a.plan.width;
     const T *kg = static_cast<const T *>(a.k);
@@ -385,10 +378,11 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(AttnArgs a, int use
     const int4 meta = a.plan.qmeta[qi];
     const int seq = meta.x, pos = meta.y;
     const int ps = a.plan.page_size;
-    const int64_t n = a.causal ? (int64_t)pos + 1 : (int64_t)a.plan.seq_lens[seq];
+    int64_t lo, hi;
+    visible_range(pos, a.plan.seq_lens[seq], a.causal, a.window, lo, hi);
     const int kvh = h / (a.hq / a.hkv);
     int64_t j0, j1;
-    split_bounds(n, a.splits, split, ps, j0, j1);
+    split_bounds(lo, hi, a.splits, split, ps, j0, j1);
     const int32_t *trow = a.plan.table + (int64_t)seq * a.plan.width;
     const T *kg = static_cast<const T *>(a.k);
     const T *vg = static_cast<const T *>(a.v);

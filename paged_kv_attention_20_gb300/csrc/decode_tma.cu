@@ -52,14 +52,6 @@ template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-__device__ __forceinline__ void split_bounds(int64_t n, int splits, int s, int ps, int64_t &j0, int64_t &j1) {
-    int64_t chunk = (n + splits - 1) / splits;
-    chunk = (chunk + ps - 1) / ps * ps;
-    int64_t b = (int64_t)s * chunk, e = b + chunk;
-    j0 = b < n ? b : n;
-    j1 = e < n ? e : n;
-}
-
 template <int D, int GH>
 struct Cfg {
     static constexpr int NW = 4;                               // warps per CTA
@@ -143,12 +135,16 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
     const int4 meta = a.plan.qmeta[qi];
     const int seq = meta.x, pos = meta.y;
     const int ps = a.plan.page_size;
-    const int64_t n = a.causal ? (int64_t)pos + 1 : (int64_t)a.plan.seq_lens[seq];
+    int64_t lo, hi;
+    visible_range(pos, a.plan.seq_lens[seq], a.causal, a.window, lo, hi);
     const int kvh = hg / tp.groups;
     const int h0 = kvh * (a.hq / a.hkv) + (hg % tp.groups) * GH;
     int64_t j0, j1;
-    split_bounds(n, a.splits, split, ps, j0, j1);
-    const int ntiles = (int)((j1 - j0 + C::TT - 1) / C::TT);
+    split_bounds(lo, hi, a.splits, split, ps, j0, j1);
+    // Tiles start on a multiple of TT (so no TMA box crosses a page); keys of the
+    // first tile below j0 (only under a sliding window) are masked.
+    const int64_t jb = j0 < j1 ? j0 / C::TT * C::TT : j0;
+    const int ntiles = (int)((j1 - jb + C::TT - 1) / C::TT);
     const int mine = ntiles > warp ? (ntiles - warp + C::NW - 1) / C::NW : 0;
     const int32_t *trow = a.plan.table + (int64_t)seq * a.plan.width;
     const int used_pages = (a.plan.seq_lens[seq] + ps - 1) >> tp.ps_shift;
@@ -165,7 +161,7 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
         const int st = i % C::NST;
         uint8_t *kdst = ring + st * C::STAGE;
         uint8_t *vdst = kdst + C::TILE;
-        const int64_t jt = j0 + (int64_t)(warp + i * C::NW) * C::TT;
+        const int64_t jt = jb + (int64_t)(warp + i * C::NW) * C::TT;
         mbar_arrive_expect_tx(&bars[st], C::STAGE);
         for (int b = 0; b < C::TT; b += tp.box_rows) {
             const int64_t j = jt + b;
@@ -221,8 +217,9 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
         if (!ok) break;
         const uint8_t *K = ring + st * C::STAGE;
         const uint8_t *V = K + C::TILE;
-        const int64_t jt = j0 + (int64_t)(warp + i * C::NW) * C::TT;
+        const int64_t jt = jb + (int64_t)(warp + i * C::NW) * C::TT;
         const int valid = (int)((j1 - jt) < C::TT ? (j1 - jt) : C::TT);
+        const int first = (int)(j0 > jt ? j0 - jt : 0);     // keys below j0 (first tile only)
 
         // scores
 #pragma unroll
@@ -261,7 +258,7 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
         for (int k = 0; k < HP; ++k) {
             const int g = 2 * k + (lane >> 4);
             const bool gv = g < GH;
-            const float s = (gv && t16 < valid) ? sp[2 * C::TT * GH + t16 * GH + g] : -INFINITY;
+            const float s = (gv && t16 < valid && t16 >= first) ? sp[2 * C::TT * GH + t16 * GH + g] : -INFINITY;
             float alpha = 1.f;
             if (__any_sync(0xffffffffu, s > m_ref[k] + kSlack)) {
                 float mt = s;

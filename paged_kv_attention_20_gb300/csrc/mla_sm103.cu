@@ -18,8 +18,11 @@
 // once, by the CTA that owns its columns; the same 128-byte-swizzled tile is
 // the K-major B operand of Q.K^T and the MN-major B operand of P.V.
 //
-// Roles per CTA: warps 0-3 exchange/softmax/epilogue (thread r = head r, TMEM
-// lane r), warp 4 TMA producer (64-key tiles, 3 stages), warp 5 MMA issuer.
+// Roles per CTA: warps 0-3 softmax/epilogue (thread r = head r, TMEM lane r),
+// warp 4 TMA producer (64-key tiles, 3 stages), warp 5 MMA issuer, warps 6-9
+// senders: they read each partial score tile from TMEM and push it to the
+// peer, so the SM-to-SM transfer (the slowest link: ~20 GB/s per SM each
+// way) of tile kt+1 overlaps the softmax of tile kt.
 // The CTA's 256 latent columns of Q live in TMEM (the A operand of Q.K^T is
 // read from there), which leaves shared memory for three latent stages; the
 // 64 position columns of Q stay in shared memory on CTA 0.  P (16-bit) is
@@ -50,7 +53,7 @@ constexpr int kR = 512;                   // latent rank
 constexpr int kP = 64;                    // rotary position dims
 constexpr int kN = 64;                    // keys per tile
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;              // 4 softmax + producer + MMA + 4 sender warps
 constexpr int kBlk = kHeads * 128;        // one 64-column block of the Q tile (bytes)
 constexpr int kKBlk = kN * 128;           // one 64-column block of a key tile (bytes)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -66,6 +69,7 @@ struct Smem {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t s_full[2];                  // S of tile kt in TMEM buffer kt % 2
+    uint64_t s_sent[2];                  // the sender warps have read S of tile kt (P may overwrite it)
     uint64_t p_ready;
     uint64_t o_done[2];                  // P.V of tile kt done -> o_done[kt % 2]
     uint64_t recv_full[2];               // local expect_tx + the peer's asynchronous stores (bytes)
@@ -90,6 +94,7 @@ struct MlaParams {
     int ps_shift;
     float scale_log2;
     int causal;
+    int window;
     int bf16;
 };
 
@@ -151,14 +156,6 @@ __device__ __forceinline__ bool wait_cluster(uint64_t *bar, uint32_t parity, lon
     return true;
 }
 
-__device__ __forceinline__ void split_bounds(int64_t n, int splits, int s, int ps, int64_t &j0, int64_t &j1) {
-    int64_t chunk = (n + splits - 1) / splits;
-    chunk = (chunk + ps - 1) / ps * ps;
-    int64_t b = (int64_t)s * chunk, e = b + chunk;
-    j0 = b < n ? b : n;
-    j1 = e < n ? e : n;
-}
-
 template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);
 template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -190,10 +187,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int seq = meta.x, pos = meta.y;
     const int ps = prm.plan.page_size;
     const int seq_len = prm.plan.seq_lens[seq];
-    const int64_t n = prm.causal ? (int64_t)pos + 1 : (int64_t)seq_len;
+    int64_t lo, hi;
+    visible_range(pos, seq_len, prm.causal, prm.window, lo, hi);
     int64_t j0, j1;
-    split_bounds(n, prm.splits, split, ps, j0, j1);
-    const int n_kt = (int)((j1 - j0 + kN - 1) / kN);
+    split_bounds(lo, hi, prm.splits, split, ps, j0, j1);
+    // Key tiles start on a multiple of 64 (no TMA box crosses a page); keys of
+    // the first tile below j0 (only under a sliding window) are masked.
+    const int64_t jb = j0 < j1 ? j0 / kN * kN : j0;
+    const int n_kt = (int)((j1 - jb + kN - 1) / kN);
     const int32_t *trow = prm.plan.table + (int64_t)seq * prm.plan.width;
 
     if (tid == 0) {
@@ -205,6 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.s_full[i], 1);
+            mbar_init(&s.s_sent[i], 4);
             mbar_init(&s.o_done[i], 1);
         }
         mbar_init(&s.p_ready, kHeads);
@@ -245,7 +247,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(&s.kv_full[st], (uint32_t)(rank == 0 ? 5 : 4) * kKBlk);
-                const int64_t jt = j0 + (int64_t)kt * kN;
+                const int64_t jt = jb + (int64_t)kt * kN;
                 for (int b = 0; b < kN; b += prm.box_rows) {
                     const int64_t j = jt + b;
                     const int64_t lp = j >> prm.ps_shift;
@@ -303,19 +305,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 atomicCAS(prm.status, 0, PA_DEVICE_TIMEOUT_MMA);
             }
         }
-    } else {
-        // ------------------------------- exchange / softmax / epilogue rows --
-        // Per tile: read the partial scores from TMEM, send them to the peer
-        // (double-buffered receive, so the peer can run a tile ahead), add the
-        // peer's partial, softmax, P into TMEM.
-        const int r = tid;
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        // peer addresses of receive buffer b (and its barriers): base + b * stride
+    } else if (warp >= 6) {
+        // --------------------------------------------------------- senders --
+        // Warp w reads TMEM lane quarter w % 4 (rows 32*(w%4)..): each partial
+        // score tile goes to the peer's recv[kt & 1] by asynchronous remote
+        // stores that complete bytes on the peer's recv_full barrier.
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         const uint32_t recv_peer0 = peer_addr(smem_u32(&s.recv[0][r * kN]), peer);
         const uint32_t recv_full_peer0 = peer_addr(smem_u32(&s.recv_full[0]), peer);
+        const int sw = r & 15;                   // chunk swizzle of row r
+        bool ok = true;
+        for (int kt = 0; ok && kt < n_kt; ++kt) {
+            const int b = kt & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[b], (kt / 2) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            float sc[kN];
+#pragma unroll
+            for (int c = 0; c < kN; c += 32) tmem_ld32f(tmem_s(b) + lane_off + c, sc + c);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.s_sent[b]);
+            // the peer has read what this buffer held two tiles ago
+            if (kt >= 2) ok = __all_sync(0xffffffffu, wait_cluster(&s.can_send[b], ((kt / 2) - 1) & 1));
+            if (!ok) break;
+            const uint32_t dst = recv_peer0 + (uint32_t)b * (uint32_t)sizeof(s.recv[0]);
+#pragma unroll
+            for (int c = 0; c < kN / 4; ++c)
+                st_async_v4(dst + ((c ^ sw) * 16), sc[4 * c], sc[4 * c + 1], sc[4 * c + 2], sc[4 * c + 3],
+                            recv_full_peer0 + (uint32_t)b * 8u);
+        }
+        if (!ok) {
+            atomicExch(&s.abort, 1);
+            atomicCAS(prm.status, 0, PA_DEVICE_TIMEOUT_SOFTMAX);
+        }
+    } else {
+        // ---------------------------------------- softmax / epilogue rows --
+        // Per tile: own partial scores from TMEM plus the peer's from recv,
+        // softmax, P into TMEM over the S columns (once the senders have read them).
+        const int r = tid;
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
         const uint32_t can_send_peer0 = peer_addr(smem_u32(&s.can_send[0]), peer);
-        auto recv_peer = [&](int b) { return recv_peer0 + (uint32_t)b * (uint32_t)sizeof(s.recv[0]); };
-        auto recv_full_peer = [&](int b) { return recv_full_peer0 + (uint32_t)b * 8u; };
         auto can_send_peer = [&](int b) { return can_send_peer0 + (uint32_t)b * 8u; };
         const int sw = r & 15;                   // chunk swizzle of row r
         {
@@ -340,29 +373,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         float cur[kN];
-        // read partial scores of tile t from TMEM and send them to the peer's recv[t & 1]
-        auto fetch_and_send = [&](int t, float (&sc)[kN]) -> bool {
-            const int b = t & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&s.s_full[t & 1], (t / 2) & 1))) return false;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < kN; c += 32) tmem_ld32f(tmem_s(t & 1) + lane_off + c, sc + c);
-            tmem_wait_ld();
-            if (r == 0) mbar_arrive_expect_tx(&s.recv_full[b], kHeads * kN * 4);   // my receive of tile t
-            if (t >= 2 && !__all_sync(0xffffffffu, wait_cluster(&s.can_send[b], ((t / 2) - 1) & 1))) return false;
-#pragma unroll
-            for (int c = 0; c < kN / 4; ++c)
-                st_async_v4(recv_peer(b) + ((c ^ sw) * 16), sc[4 * c], sc[4 * c + 1], sc[4 * c + 2], sc[4 * c + 3],
-                            recv_full_peer(b));
-            return true;
-        };
         for (int kt = 0; ok && kt < n_kt; ++kt) {
             const int sb = kt & 1;         // receive buffer
             const int pb = kt & 1;         // S / P buffer
-            const int64_t kbase = j0 + (int64_t)kt * kN;
+            const int64_t kbase = jb + (int64_t)kt * kN;
             const int valid = (int)((j1 - kbase) < kN ? (j1 - kbase) : kN);
-            ok = fetch_and_send(kt, cur);
+            const int first = (int)(j0 > kbase ? j0 - kbase : 0);      // keys below j0 (first tile only)
+            if (r == 0) mbar_arrive_expect_tx(&s.recv_full[sb], kHeads * kN * 4);   // my receive of tile kt
+            ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[pb], (kt / 2) & 1));
             if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < kN; c += 32) tmem_ld32f(tmem_s(pb) + lane_off + c, cur + c);
+            tmem_wait_ld();
             ok = __all_sync(0xffffffffu, wait_cluster(&s.recv_full[sb], (kt / 2) & 1));
             if (!ok) break;
             const float *mine = &s.recv[sb][r * kN];
@@ -374,10 +397,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 cur2[2 * c + 1] = fadd2(cur2[2 * c + 1], make_float2(o.z, o.w));
             }
             // online softmax (identical on both CTAs); keys past the visible range score -inf
-            if (valid < kN) {
+            if (valid < kN || first > 0) {
 #pragma unroll
                 for (int c = 0; c < kN; ++c)
-                    if (c >= valid) cur[c] = -INFINITY;
+                    if (c >= valid || c < first) cur[c] = -INFINITY;
             }
             float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
@@ -410,6 +433,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
             }
+            // the senders must have read S before P overwrites it
+            ok = __all_sync(0xffffffffu, mbar_wait(&s.s_sent[pb], (kt / 2) & 1));
+            if (!ok) break;
+            tc_fence_after();
             // P = exp2(s * scale - m_ref) as 16-bit pairs over this row's S columns
             // (already read); every tile has a visible key, so m_ref is finite here
             const float2 sc2 = make_float2(prm.scale_log2, prm.scale_log2);
@@ -548,6 +575,7 @@ cudaError_t launch_mla(const AttnArgs &a, bool use_list, cudaStream_t st) {
     prm.ps_shift = log2_exact(ps);
     prm.scale_log2 = a.scale * kLog2e;
     prm.causal = a.causal;
+    prm.window = a.window;
     prm.bf16 = bf16 ? 1 : 0;
     const uint64_t rows = (uint64_t)a.plan.pages * ps;
     CUtensorMap tqp, tlat, tkp;

@@ -53,8 +53,8 @@ cudaError_t scratch_address(void **out) {
 extern "C" pa_status paged_attn_forward_split_static(const pa_plan *plan, const void *q, const void *k_cache,
                                                      const void *v_cache, void *out, int32_t num_heads,
                                                      int32_t num_kv_heads, int32_t head_dim, int32_t value_dim,
-                                                     float scale, int32_t causal, pa_dtype dtype, int32_t splits,
-                                                     pa_stream_t stream) {
+                                                     float scale, int32_t causal, int32_t window, pa_dtype dtype,
+                                                     int32_t splits, pa_stream_t stream) {
     int64_t counts[8];
     pa_status st = pa_plan_describe(plan, counts);
     if (st != PA_OK) return st;
@@ -73,5 +73,6 @@ extern "C" pa_status paged_attn_forward_split_static(const pa_plan *plan, const 
         return pa_fail_with(PA_ERR_CUDA, "paged_attn_forward_split_static: cudaGetSymbolAddress of the static "
                                          "scratch failed");
     return paged_attn_forward_split(plan, q, k_cache, v_cache, out, num_heads, num_kv_heads, head_dim, value_dim,
-                                    scale, causal, dtype, scratch, (size_t)PA_STATIC_SCRATCH_BYTES, splits, stream);
+                                    scale, causal, window, dtype, scratch, (size_t)PA_STATIC_SCRATCH_BYTES, splits,
+                                    stream);
 }

@@ -45,10 +45,42 @@ struct AttnArgs {
     int32_t hq, hkv, d, dv, p;
     float scale;
     int32_t causal;
+    int32_t window;       // sliding window (0 = none): keys pos - window + 1 and later
     int32_t splits;
     pa_dtype dtype;
     int32_t *status;      // device status word (bounded waits record timeouts here)
 };
+
+// Keys a query at absolute position `pos` of a sequence holding `seq_len`
+// keys may see: [lo, hi).  hi is pos + 1 (causal) or seq_len; a sliding
+// window W > 0 (a layer's `window`, libmir-cuda 0.1.0,
+// src/backend/attention/graph/mod.rs, `Geometry`) raises lo to pos - W + 1.
+__host__ __device__ inline void visible_range(int pos, int seq_len, int causal, int window, int64_t &lo,
+                                              int64_t &hi) {
+    hi = causal ? (int64_t)pos + 1 : (int64_t)seq_len;
+    lo = window > 0 ? (int64_t)pos - window + 1 : 0;
+    if (lo < 0) lo = 0;
+}
+
+// Split s of `splits` over the visible keys [lo, hi): with base = lo rounded
+// down to a page boundary and chunk = ceil((hi - base) / splits) rounded up to
+// a page multiple, split s covers [max(lo, base + s*chunk), min(base + (s+1)*chunk, hi)).
+// Every split but the first starts on a page boundary; an empty split has j0 == j1.
+__host__ __device__ inline void split_bounds(int64_t lo, int64_t hi, int splits, int s, int ps, int64_t &j0,
+                                             int64_t &j1) {
+    const int64_t base = lo / ps * ps;
+    int64_t n = hi - base;
+    if (n < 0) n = 0;
+    int64_t chunk = (n + splits - 1) / splits;
+    chunk = (chunk + ps - 1) / ps * ps;
+    int64_t b = base + (int64_t)s * chunk, e = b + chunk;
+    if (b < lo) b = lo;
+    if (b > hi) b = hi;
+    if (e > hi) e = hi;
+    if (e < b) e = b;
+    j0 = b;
+    j1 = e;
+}
 
 // Launchers (return cudaGetLastError() of the launch).
 // use_decode_list: iterate over plan.decode (else over every query).

@@ -273,7 +273,7 @@ size_t pa_workspace_bytes(int32_t queries, int32_t heads, int32_t value_dim, int
 }
 
 int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t num_kv_heads,
-                                   int32_t num_sms) {
+                                   int32_t window, int32_t num_sms) {
     if (!plan || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads || num_sms < 1) return 1;
     int64_t items = plan->n_decode;
     if (items == 0) return 1;
@@ -281,13 +281,14 @@ int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32
     int64_t blocks = items * num_kv_heads * ((group + 7) / 8);
     int64_t target = 4 * (int64_t)num_sms;
     int64_t s = (target + blocks - 1) / blocks;
-    int64_t cap = std::max<int64_t>(1, plan->max_seq_len / (4 * (int64_t)plan->page_size));
+    const int64_t longest = window > 0 ? std::min<int64_t>(plan->max_seq_len, window) : plan->max_seq_len;
+    int64_t cap = std::max<int64_t>(1, longest / (4 * (int64_t)plan->page_size));
     s = std::min<int64_t>(s, cap);
     s = std::max<int64_t>(1, std::min<int64_t>(s, PA_MAX_SPLITS));
     return (int32_t)s;
 }
 
-int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t num_sms) {
+int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t window, int32_t num_sms) {
     if (!plan || num_heads < 1 || num_sms < 1 || plan->queries == 0) return 1;
     // one CTA pair per (query, 128 heads, split); aim for about two waves of SMs
     const int64_t pairs = (int64_t)plan->queries * ((num_heads + 127) / 128);
@@ -295,6 +296,7 @@ int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_
     int64_t longest = 0;
     for (int32_t q = 0; q < plan->queries; ++q)
         longest = std::max<int64_t>(longest, (int64_t)plan->words[plan->off_qmeta + 4 * (size_t)q + 1] + 1);
+    if (window > 0) longest = std::min<int64_t>(longest, window);
     const int64_t cap = std::max<int64_t>(1, longest / 256);   // splits of at least 4 tiles of 64 keys
     s = std::max<int64_t>(1, std::min<int64_t>(std::min(s, cap), PA_MAX_SPLITS));
     return (int32_t)s;
@@ -325,7 +327,7 @@ namespace {
 // Shared body of the attention entry points.
 pa_status attention(const pa_plan *plan, const void *q, const void *k, const void *v, const void *qp,
                     const void *kp, void *out, int32_t hq, int32_t hkv, int32_t d, int32_t dv, int32_t p,
-                    float scale, int32_t causal, pa_dtype dtype, void *ws, size_t ws_bytes, int32_t splits,
+                    float scale, int32_t causal, int32_t window, pa_dtype dtype, void *ws, size_t ws_bytes, int32_t splits,
                     bool split_call, bool mla, cudaStream_t st, const char *name) {
     char msg[256];
     auto bad = [&](pa_status s, const char *what) {
@@ -339,6 +341,7 @@ pa_status attention(const pa_plan *plan, const void *q, const void *k, const voi
     if (d > PA_MAX_HEAD_DIM || dv > PA_MAX_HEAD_DIM) return bad(PA_ERR_LIMIT, "head dim above 1024");
     if (!std::isfinite(scale) || !(scale > 0.f)) return bad(PA_ERR_SHAPE, "scale must be finite and > 0");
     if (causal != 0 && causal != 1) return bad(PA_ERR_ARG, "causal must be 0 or 1");
+    if (window < 0) return bad(PA_ERR_ARG, "window must be >= 0");
     if (mla) {
         if (p < 1 || p > PA_MAX_POS_DIM) return bad(PA_ERR_LIMIT, "MLA position dim must be in 1..256");
     }
@@ -365,7 +368,7 @@ pa_status attention(const pa_plan *plan, const void *q, const void *k, const voi
     a.plan = view_of(plan);
     a.q = q; a.k = k; a.v = v; a.qp = qp; a.kp = kp; a.out = out;
     a.hq = hq; a.hkv = hkv; a.d = d; a.dv = dv; a.p = mla ? p : 0;
-    a.scale = scale; a.causal = causal; a.splits = splits; a.dtype = dtype;
+    a.scale = scale; a.causal = causal; a.window = window; a.splits = splits; a.dtype = dtype;
     a.status = pa::device_status_ptr();
     if (!a.status) return bad(PA_ERR_CUDA, "device status word unavailable");
     if (splits > 1) {
@@ -416,32 +419,32 @@ extern "C" {
 
 pa_status paged_attn_forward(const pa_plan *plan, const void *q, const void *k_cache, const void *v_cache,
                              void *out, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                             int32_t value_dim, float scale, int32_t causal, pa_dtype dtype,
+                             int32_t value_dim, float scale, int32_t causal, int32_t window, pa_dtype dtype,
                              pa_stream_t stream) {
     return attention(plan, q, k_cache, v_cache, nullptr, nullptr, out, num_heads, num_kv_heads, head_dim,
-                     value_dim, 0, scale, causal, dtype, nullptr, 0, 1, false, false, (cudaStream_t)stream,
+                     value_dim, 0, scale, causal, window, dtype, nullptr, 0, 1, false, false, (cudaStream_t)stream,
                      "paged_attn_forward");
 }
 
 pa_status paged_attn_forward_split(const pa_plan *plan, const void *q, const void *k_cache,
                                    const void *v_cache, void *out, int32_t num_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t value_dim, float scale, int32_t causal,
-                                   pa_dtype dtype, void *workspace, size_t workspace_bytes, int32_t splits,
-                                   pa_stream_t stream) {
+                                   int32_t window, pa_dtype dtype, void *workspace, size_t workspace_bytes,
+                                   int32_t splits, pa_stream_t stream) {
     if (!workspace) return fail(PA_ERR_WORKSPACE, "paged_attn_forward_split: workspace is null");
     return attention(plan, q, k_cache, v_cache, nullptr, nullptr, out, num_heads, num_kv_heads, head_dim,
-                     value_dim, 0, scale, causal, dtype, workspace, workspace_bytes, splits, true, false,
+                     value_dim, 0, scale, causal, window, dtype, workspace, workspace_bytes, splits, true, false,
                      (cudaStream_t)stream, "paged_attn_forward_split");
 }
 
 pa_status paged_mla_forward(const pa_plan *plan, const void *q, const void *qp, const void *latent_cache,
                             const void *pos_cache, void *out, int32_t num_heads, int32_t latent_dim,
-                            int32_t pos_dim, float scale, int32_t causal, pa_dtype dtype, void *workspace,
-                            size_t workspace_bytes, int32_t splits, pa_stream_t stream) {
+                            int32_t pos_dim, float scale, int32_t causal, int32_t window, pa_dtype dtype,
+                            void *workspace, size_t workspace_bytes, int32_t splits, pa_stream_t stream) {
     if (!workspace && splits != 1)
         return fail(PA_ERR_SPLITS, "paged_mla_forward: splits must be 1 without a workspace");
     return attention(plan, q, latent_cache, latent_cache, qp, pos_cache, out, num_heads, 1, latent_dim,
-                     latent_dim, pos_dim, scale, causal, dtype, workspace, workspace_bytes, splits, true, true,
+                     latent_dim, pos_dim, scale, causal, window, dtype, workspace, workspace_bytes, splits, true, true,
                      (cudaStream_t)stream, "paged_mla_forward");
 }
 

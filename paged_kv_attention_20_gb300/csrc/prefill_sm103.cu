@@ -75,6 +75,7 @@ struct PrefillParams {
     int hq, hkv;
     float scale_log2;
     int causal;
+    int window;
     int bf16;
 };
 
@@ -111,7 +112,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seq_len = prm.plan.seq_lens[seq];
     const int last_pos = pos0 + nq - 1;
     const int n_keys = prm.causal ? last_pos + 1 : seq_len;
-    const int n_kt = (n_keys + kN - 1) / kN;
+    // Key tiles kt0 .. kt0 + n_kt - 1; under a sliding window the tile's first
+    // query (the lowest position) sees keys from pos0 - window + 1 on.
+    const int lo0 = prm.window > 0 ? max(0, pos0 - prm.window + 1) : 0;
+    const int kt0 = lo0 / kN;
+    const int n_kt = max(0, (n_keys + kN - 1) / kN - kt0);
     const int32_t *trow = prm.plan.table + (int64_t)seq * prm.plan.width;
 
     if (tid == 0) {
@@ -170,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
             if (!go) break;
             if (lane < pages_per_tile) {
-                const int lp = kt * pages_per_tile + lane;
+                const int lp = (kt0 + kt) * pages_per_tile + lane;
                 const int row = lp < used_pages ? trow[lp] * ps : oob_row;
                 const uint32_t off = (uint32_t)lane * ps * 128;
                 tma_load_3d(s.k[st] + off, &tm_k, 0, kvh, row, &s.kv_full[st]);
@@ -232,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col0 = 64 * h2;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         const int my_pos = pos0 + r;
-        const int vis_end = prm.causal ? min(my_pos + 1, seq_len) : seq_len;  // keys [0, vis_end)
+        const int vis_end = prm.causal ? min(my_pos + 1, seq_len) : seq_len;  // keys [vis_lo, vis_end)
+        const int vis_lo = prm.window > 0 ? max(0, my_pos - prm.window + 1) : 0;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         int xphase = 0;
@@ -252,17 +258,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[sb], (kt / 3) & 1));
             if (!ok) break;
             tc_fence_after();
-            const int kbase = kt * kN + col0;
+            const int kbase = (kt0 + kt) * kN + col0;
             // my 64 scores of the row into registers (two loads, one wait)
             uint32_t sv[64];
             tmem_ld32(tmem_s(sb) + lane_off + col0, sv);
             tmem_ld32(tmem_s(sb) + lane_off + col0 + 32, sv + 32);
             tmem_wait_ld();
-            // keys at or past the row's visible end score -inf (diagonal and sequence-end tiles only)
-            if (kbase + 64 > vis_end) {
+            // keys outside the row's visible range score -inf (diagonal, sequence-end
+            // and window-edge tiles only)
+            if (kbase + 64 > vis_end || kbase < vis_lo) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
-                    if (kbase + c >= vis_end) sv[c] = 0xff800000u;
+                    if (kbase + c >= vis_end || kbase + c < vis_lo) sv[c] = 0xff800000u;
             }
             // row maximum of the raw scores (the scale is positive, so it commutes with max)
             float ma = -INFINITY, mb = -INFINITY;
@@ -298,10 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
             }
             // P = exp2(s * scale - m_ref) as 16-bit pairs over my S columns (already in
-            // registers); masked keys hold -inf and give 0.  Every row sees key 0, so
-            // m_ref is finite from the first tile on.
+            // registers); masked keys hold -inf and give 0.  A row whose window has
+            // not started yet still has m_ref = -inf: its weights are all 0.
             const float2 sc2 = make_float2(prm.scale_log2, prm.scale_log2);
-            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            const float mr = m_ref == -INFINITY ? 0.f : m_ref;
+            const float2 nm2 = make_float2(-mr, -mr);
             float2 ls2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < 64; c += 32) {
@@ -319,11 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             l = l * alpha + (ls2.x + ls2.y);
             // V rows at or past the sequence end (tail slots) must not reach the MMA
-            if (kt * kN + kN > seq_len) {
+            if ((kt0 + kt) * kN + kN > seq_len) {
                 const int st = kt % kStages;
                 ok = __all_sync(0xffffffffu, mbar_wait(&s.kv_full[st], (kt / kStages) & 1));
                 if (!ok) break;
-                if (kt * kN + r >= seq_len) {
+                if ((kt0 + kt) * kN + r >= seq_len) {
                     const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
@@ -407,6 +415,7 @@ cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {
     prm.hkv = a.hkv;
     prm.scale_log2 = a.scale * kLog2e;
     prm.causal = a.causal;
+    prm.window = a.window;
     prm.bf16 = bf16 ? 1 : 0;
     const dim3 grid((unsigned)(a.plan.n_tiles * a.hq));
     cudaError_t e;

@@ -41,7 +41,7 @@ def plan_for(case, device="cuda"):
                                case.page_size, case.num_pages, device=device)
 
 
-def gpu_store_and_attend(case, splits=None, workspace=None, causal=None, device="cuda"):
+def gpu_store_and_attend(case, splits=None, workspace=None, causal=None, device="cuda", window=0):
     """Append the case's new rows, then attend.  Returns (out_cpu, k_cache_cpu, v_cache_cpu, plan)."""
     dc = case.to(device)
     plan = plan_for(case, device)
@@ -49,18 +49,19 @@ def gpu_store_and_attend(case, splits=None, workspace=None, causal=None, device=
     causal = case.causal if causal is None else causal
     if case.is_mla:
         out = pka.paged_mla_forward(plan, dc.q, dc.qp, dc.k_cache, dc.v_cache, case.scale, causal=causal,
-                                    workspace=workspace, splits=splits or 1)
+                                    workspace=workspace, splits=splits or 1, window=window)
     elif splits is None:
-        out = pka.paged_attn_forward(plan, dc.q, dc.k_cache, dc.v_cache, case.scale, causal=causal)
+        out = pka.paged_attn_forward(plan, dc.q, dc.k_cache, dc.v_cache, case.scale, causal=causal,
+                                     window=window)
     else:
         out = pka.paged_attn_forward_split(plan, dc.q, dc.k_cache, dc.v_cache, case.scale, splits,
-                                           workspace=workspace, causal=causal)
+                                           workspace=workspace, causal=causal, window=window)
     torch.cuda.synchronize()
     assert pka.device_status() == 0, "a device-side wait timed out"
     return out.cpu(), dc.k_cache.cpu(), dc.v_cache.cpu(), plan
 
 
-def oracle_after_store(case, rows=None, causal=None, nthreads=0):
+def oracle_after_store(case, rows=None, causal=None, nthreads=0, window=0):
     """Oracle: host append of the new rows, then fp64 attention (optionally on sampled rows)."""
     kc, vc = oracle.kv_store(case.new_k, case.new_v, case.k_cache, case.v_cache, case.block_table,
                              case.query_seq, case.query_pos)
@@ -68,10 +69,11 @@ def oracle_after_store(case, rows=None, causal=None, nthreads=0):
     if case.is_mla:
         out, lse = oracle.attention(case.q, kc, kc, case.seq_lens, case.block_table, case.query_seq,
                                     case.query_pos, case.scale, causal=causal, qp=case.qp, kp_cache=vc,
-                                    rows=rows, nthreads=nthreads)
+                                    rows=rows, nthreads=nthreads, window=window)
     else:
         out, lse = oracle.attention(case.q, kc, vc, case.seq_lens, case.block_table, case.query_seq,
-                                    case.query_pos, case.scale, causal=causal, rows=rows, nthreads=nthreads)
+                                    case.query_pos, case.scale, causal=causal, rows=rows, nthreads=nthreads,
+                                    window=window)
     return out, lse, kc, vc
 
 

@@ -33,7 +33,7 @@ def test_header_functions_are_exported(built_lib):
     for n in names:
         assert hasattr(built_lib, n), f"{n} declared in paged_attn.h but not exported"
     assert set(pka.EXPORTED) <= set(names)
-    assert built_lib.pa_abi_version() == 1
+    assert built_lib.pa_abi_version() == 2
 
 
 def _status_of(fn, *a, **k):
@@ -114,6 +114,9 @@ def test_split_heuristic(built_lib):
     assert 8 <= s <= 64
     small = plan([20], [[0, 1]], [0], [19], 16, 2)
     assert pka.paged_attn_split_heuristic(small, 8, 8, num_sms=152) == 1   # one page: no split
+    # a sliding window bounds the history the heuristic splits
+    assert pka.paged_attn_split_heuristic(p, 64, 8, num_sms=152, window=64) == 1
+    assert pka.paged_attn_split_heuristic(p, 64, 8, num_sms=152, window=4096) <= 4096 // 64
 
 
 def _lib():
@@ -127,23 +130,25 @@ def test_attention_argument_checks_before_launch(built_lib):
     h = p.handle
     fake = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails validation first
     f = lib.paged_attn_forward
-    assert f(h, fake, fake, fake, fake, 6, 4, 64, 64, 0.1, 1, 2, None) == 2          # Hq % Hkv
-    assert f(h, fake, fake, fake, fake, 0, 1, 64, 64, 0.1, 1, 2, None) == 2          # Hq == 0
-    assert f(h, fake, fake, fake, fake, 4, 4, 1025, 64, 0.1, 1, 2, None) == 8        # d > 1024
-    assert f(h, fake, fake, fake, fake, 4, 4, 64, 0, 0.1, 1, 2, None) == 2           # dv == 0
-    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, float("nan"), 1, 2, None) == 2  # scale NaN
-    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, -1.0, 1, 2, None) == 2         # scale <= 0
-    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 7, None) == 3          # dtype
-    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, None) == 10         # not uploaded
+    assert f(h, fake, fake, fake, fake, 6, 4, 64, 64, 0.1, 1, 0, 2, None) == 2          # Hq % Hkv
+    assert f(h, fake, fake, fake, fake, 0, 1, 64, 64, 0.1, 1, 0, 2, None) == 2          # Hq == 0
+    assert f(h, fake, fake, fake, fake, 4, 4, 1025, 64, 0.1, 1, 0, 2, None) == 8        # d > 1024
+    assert f(h, fake, fake, fake, fake, 4, 4, 64, 0, 0.1, 1, 0, 2, None) == 2           # dv == 0
+    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, float("nan"), 1, 0, 2, None) == 2  # scale NaN
+    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, -1.0, 1, 0, 2, None) == 2         # scale <= 0
+    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 0, 7, None) == 3          # dtype
+    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, -1, 2, None) == 1         # window < 0
+    assert f(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 0, 2, None) == 10         # not uploaded
     fs = lib.paged_attn_forward_split
-    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, fake, 1 << 20, 65, None) == 7
-    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, fake, 1 << 20, 0, None) == 7
-    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, fake, 16, 4, None) == 6   # too small
-    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, None, 1 << 20, 4, None) == 6
+    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 0, 2, fake, 1 << 20, 65, None) == 7
+    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 0, 2, fake, 1 << 20, 0, None) == 7
+    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 0, 2, fake, 16, 4, None) == 6   # too small
+    assert fs(h, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 0, 2, None, 1 << 20, 4, None) == 6
     m = lib.paged_mla_forward
-    assert m(h, fake, fake, fake, fake, fake, 4, 64, 0, 0.1, 1, 2, None, 0, 1, None) == 8     # P == 0
-    assert m(h, fake, fake, fake, fake, fake, 4, 64, 257, 0.1, 1, 2, None, 0, 1, None) == 8   # P > 256
-    assert m(h, fake, fake, fake, fake, fake, 4, 64, 64, 0.1, 1, 2, None, 0, 2, None) == 7    # split w/o ws
+    assert m(h, fake, fake, fake, fake, fake, 4, 64, 0, 0.1, 1, 0, 2, None, 0, 1, None) == 8     # P == 0
+    assert m(h, fake, fake, fake, fake, fake, 4, 64, 257, 0.1, 1, 0, 2, None, 0, 1, None) == 8   # P > 256
+    assert m(h, fake, fake, fake, fake, fake, 4, 64, 64, 0.1, 1, 0, 2, None, 0, 2, None) == 7    # split w/o ws
+    assert m(h, fake, fake, fake, fake, fake, 4, 64, 64, 0.1, 1, -3, 2, None, 0, 1, None) == 1   # window < 0
     st = lib.paged_kv_store
     assert st(h, fake, fake, fake, fake, 0, 64, 64, 2, None) == 2
     assert st(h, fake, fake, fake, fake, 1, 64, 64, 9, None) == 3
@@ -156,7 +161,7 @@ def test_zero_queries_is_ok_without_launch(built_lib):
     lib = _lib()
     p = plan([5], [[0]], [], [], 16, 1)
     fake = ctypes.c_void_p(0x1000)
-    assert lib.paged_attn_forward(p.handle, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 2, None) == 0
+    assert lib.paged_attn_forward(p.handle, fake, fake, fake, fake, 4, 4, 64, 64, 0.1, 1, 0, 2, None) == 0
     assert lib.paged_kv_store(p.handle, fake, fake, fake, fake, 1, 64, 64, 2, None) == 0
 
 

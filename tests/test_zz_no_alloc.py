@@ -31,7 +31,7 @@ def _static_fn():
     lib = pka.load()
     fn = lib.paged_attn_forward_split_static
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
-    fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, i32, ctypes.c_int, i32, vp]
+    fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, i32, i32, ctypes.c_int, i32, vp]
     fn.restype = ctypes.c_int
     return lib, fn
 
@@ -45,7 +45,7 @@ def _run_both(case, splits):
     out = torch.full_like(ref, float("nan"))
     stream = torch.cuda.current_stream().cuda_stream
     rc = fn(plan.handle, dc.q.data_ptr(), dc.k_cache.data_ptr(), dc.v_cache.data_ptr(), out.data_ptr(),
-            case.hq, case.hkv, case.d, case.dv, case.scale, 1, 2, splits, stream)
+            case.hq, case.hkv, case.d, case.dv, case.scale, 1, 0, 2, splits, stream)
     assert rc == 0, lib.pa_last_error().decode()
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), ref.float().cpu().numpy()
@@ -71,6 +71,6 @@ def test_static_scratch_refuses_oversize(cuda_device):
     fake = ctypes.c_void_p(0x1000)   # never dereferenced: the size check fails first
     # 1 query x 1024 heads x 1024 dims x 64 splits x 4 B = 256 MiB > 16 MiB
     assert pka.workspace_bytes(1, 1024, 1024, 64) > SCRATCH_BYTES
-    rc = fn(plan.handle, fake, fake, fake, fake, 1024, 1024, 1024, 1024, 0.1, 1, 2, 64, None)
+    rc = fn(plan.handle, fake, fake, fake, fake, 1024, 1024, 1024, 1024, 0.1, 1, 0, 2, 64, None)
     assert rc == PA_ERR_WORKSPACE
     assert "PA_STATIC_SCRATCH_BYTES" in lib.pa_last_error().decode()
