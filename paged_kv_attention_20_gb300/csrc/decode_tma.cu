@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
                 for (int c = 0; c < C::CPL / 2; ++c) acc[g][c] = make_float2(acc[g][c].x * a_g, acc[g][c].y * a_g);
             }
         }
-        for (int t = 0; t < valid; ++t) {
+        auto pv_token = [&](int t) {
             uint32_t vw[C::CPL / 2];
             if constexpr (C::CPL == 8) {
                 const uint4 w = *reinterpret_cast<const uint4 *>(V + t * C::ROW + lane * 16);
@@ -316,6 +316,13 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
 #pragma unroll
                 for (int g = 0; g < GH; ++g) acc[g][c] = ffma2(pg[g], vf, acc[g][c]);
             }
+        };
+        if (valid == C::TT) {
+            // whole tile: unrolled, so the shared-memory loads of later tokens issue early
+#pragma unroll
+            for (int t = 0; t < C::TT; ++t) pv_token(t);
+        } else {
+            for (int t = 0; t < valid; ++t) pv_token(t);
         }
         __syncwarp();
         if (lane == 0 && i + C::NST < mine) {

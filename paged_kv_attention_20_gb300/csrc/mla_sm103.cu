@@ -127,16 +127,6 @@ __device__ __forceinline__ void arrive_remote(uint32_t remote_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(remote_bar) : "memory");
 }
 
-// Relaxed remote arrive (no cluster-scope fence) used to say "my receive
-// buffer has been read".  `dep` is a value computed from everything that was
-// read, so the arrive is issued only after those loads have returned.
-__device__ __forceinline__ void arrive_remote_after(uint32_t remote_bar, float dep) {
-    asm volatile("{\n .reg .b32 d;\n mov.b32 d, %1;\n mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n}\n" ::"r"(
-                     remote_bar),
-                 "f"(dep)
-                 : "memory");
-}
-
 __device__ __forceinline__ bool try_wait_cluster(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -409,9 +399,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mb = fmax3(mb, cur[c + 2], cur[c + 3]);
             }
             const float mt = fmaxf(ma, mb) * prm.scale_log2;   // the scale is positive
-            // this warp's rows of recv[sb] are read (mt depends on every loaded value)
-            const float wdep = __shfl_sync(0xffffffffu, mt, 0) + __shfl_sync(0xffffffffu, mt, 31);
-            if (lane == 0) arrive_remote_after(can_send_peer(sb), wdep);
+            // this warp's rows of recv[sb] are read: release them to the peer's
+            // senders (the release orders every lane's reads before the arrive)
+            __syncwarp();
+            if (lane == 0) arrive_remote(can_send_peer(sb));
             float alpha = 1.f;
             if (mt > m_ref + kSlack) {
                 alpha = exp2f(m_ref - mt);

@@ -118,12 +118,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kt0 = lo0 / kN;
     const int n_kt = max(0, (n_keys + kN - 1) / kN - kt0);
     const int32_t *trow = prm.plan.table + (int64_t)seq * prm.plan.width;
+    // CTAs of one cluster hold query heads of the same KV head and the same
+    // query tile: they walk the same key tiles, and each K/V tile is loaded once
+    // for all of them (multicast), every CTA issuing a share of its boxes.
+    const uint32_t crank = cluster_ctarank(), csize = cluster_nctarank();
+    const uint16_t cmask = (uint16_t)((1u << csize) - 1u);
 
     if (tid == 0) {
         mbar_init(&s.q_full, 1);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&s.kv_full[i], 1);
-            mbar_init(&s.kv_empty[i], 1);
+            mbar_init(&s.kv_empty[i], csize);      // one release per CTA of the cluster
         }
         for (int i = 0; i < 3; ++i) mbar_init(&s.s_full[i], 1);
         mbar_init(&s.p_ready, 2 * kM);
@@ -140,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_barrier();       // every barrier of the cluster exists before any multicast lands
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
     auto tmem_s = [tmem](int b) -> uint32_t { return tmem + 128u * (uint32_t)b; };   // S / P buffers 0..2
@@ -178,11 +183,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int lp = (kt0 + kt) * pages_per_tile + lane;
                 const int row = lp < used_pages ? trow[lp] * ps : oob_row;
                 const uint32_t off = (uint32_t)lane * ps * 128;
-                tma_load_3d(s.k[st] + off, &tm_k, 0, kvh, row, &s.kv_full[st]);
-                tma_load_3d(s.k[st] + kHalfBytes + off, &tm_k, 64, kvh, row, &s.kv_full[st]);
-                tma_load_3d(s.v[st] + off, &tm_v, 0, kvh, row, &s.kv_full[st]);
-                tma_load_3d(s.v[st] + kHalfBytes + off, &tm_v, 64, kvh, row, &s.kv_full[st]);
+                if (csize == 1) {
+                    tma_load_3d(s.k[st] + off, &tm_k, 0, kvh, row, &s.kv_full[st]);
+                    tma_load_3d(s.k[st] + kHalfBytes + off, &tm_k, 64, kvh, row, &s.kv_full[st]);
+                    tma_load_3d(s.v[st] + off, &tm_v, 0, kvh, row, &s.kv_full[st]);
+                    tma_load_3d(s.v[st] + kHalfBytes + off, &tm_v, 64, kvh, row, &s.kv_full[st]);
+                } else {
+                    // boxes K lo, K hi, V lo, V hi of this page: box j is issued by CTA j % csize
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if ((uint32_t)(j % (int)csize) != crank) continue;
+                        uint8_t *dst = (j < 2 ? s.k[st] : s.v[st]) + (j & 1) * kHalfBytes + off;
+                        tma_load_3d_multicast(dst, j < 2 ? &tm_k : &tm_v, (j & 1) * 64, kvh, row, &s.kv_full[st],
+                                              cmask);
+                    }
+                }
             }
+        }
+        // With a cluster, peers release stages by remote arrivals: wait for the
+        // last ones so none lands after this CTA has exited.
+        if (csize > 1 && lane == 0) {
+            for (int kt = max(0, n_kt - kStages); kt < n_kt; ++kt)
+                if (!mbar_wait(&s.kv_empty[kt % kStages], (kt / kStages) & 1)) {
+                    set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
+                    break;
+                }
         }
     } else if (warp == 9) {
         // ------------------------------------------------------ MMA issuer --
@@ -202,7 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
                 }
                 mma_commit(&s.o_done[kt % 3]);
-                mma_commit(&s.kv_empty[st]);
+                if (csize == 1)
+                    mma_commit(&s.kv_empty[st]);
+                else
+                    mma_commit_multicast(&s.kv_empty[st], cmask);   // this CTA's copy of the stage is free
                 return true;
             };
             // S runs two tiles ahead of P.V: S0, S1, then per tile P.V(kt), S(kt+2).
@@ -375,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_barrier();
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -417,27 +445,43 @@ cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {
     prm.causal = a.causal;
     prm.window = a.window;
     prm.bf16 = bf16 ? 1 : 0;
-    const dim3 grid((unsigned)(a.plan.n_tiles * a.hq));
+    // Cluster of up to 4 CTAs = query heads sharing one KV head (consecutive
+    // blocks: block = tile * Hq + head, and the group size divides Hq).
+    const int group = a.hq / a.hkv;
+    const unsigned csize = group % 4 == 0 ? 4u : group % 2 == 0 ? 2u : 1u;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(a.plan.n_tiles * a.hq));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     cudaError_t e;
     if (bf16) {
-        static bool cfg = false;
-        if (!cfg) {
+        static bool done = false;
+        if (!done) {
             e = cudaFuncSetAttribute(prefill_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemBytes);
             if (e != cudaSuccess) return e;
-            cfg = true;
+            done = true;
         }
-        prefill_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, prm);
+        e = cudaLaunchKernelEx(&cfg, prefill_kernel<__nv_bfloat16>, tq, tk, tv, prm);
     } else {
-        static bool cfg = false;
-        if (!cfg) {
+        static bool done = false;
+        if (!done) {
             e = cudaFuncSetAttribute(prefill_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemBytes);
             if (e != cudaSuccess) return e;
-            cfg = true;
+            done = true;
         }
-        prefill_kernel<__half><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, prm);
+        e = cudaLaunchKernelEx(&cfg, prefill_kernel<__half>, tq, tk, tv, prm);
     }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
