@@ -22,7 +22,8 @@
 // warp 4 TMA producer (64-key tiles, 3 stages), warp 5 MMA issuer, warps 6-9
 // senders: they read each partial score tile from TMEM and push it to the
 // peer, so the SM-to-SM transfer (the slowest link: ~20 GB/s per SM each
-// way) of tile kt+1 overlaps the softmax of tile kt.
+// way) of tile kt+1 overlaps the softmax of tile kt; warp 10 releases the
+// receive buffers to the peer.
 // The CTA's 256 latent columns of Q live in TMEM (the A operand of Q.K^T is
 // read from there), which leaves shared memory for three latent stages; the
 // 64 position columns of Q stay in shared memory on CTA 0.  P (16-bit) is
@@ -53,7 +54,7 @@ constexpr int kR = 512;                   // latent rank
 constexpr int kP = 64;                    // rotary position dims
 constexpr int kN = 64;                    // keys per tile
 constexpr int kStages = 3;
-constexpr int kThreads = 320;              // 4 softmax + producer + MMA + 4 sender warps
+constexpr int kThreads = 352;              // 4 softmax + producer + MMA + 4 sender warps + releaser
 constexpr int kBlk = kHeads * 128;        // one 64-column block of the Q tile (bytes)
 constexpr int kKBlk = kN * 128;           // one 64-column block of a key tile (bytes)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -70,10 +71,13 @@ struct Smem {
     uint64_t kv_empty[kStages];
     uint64_t s_full[2];                  // S of tile kt in TMEM buffer kt % 2
     uint64_t s_sent[2];                  // the sender warps have read S of tile kt (P may overwrite it)
-    uint64_t p_ready;
+    uint64_t p_ready[2];                 // P of tile kt in TMEM (all 128 rows) -> p_ready[kt % 2].  One
+                                         // barrier per tile in flight: softmax warps are not in step,
+                                         // and a warp already on tile kt+1 must not count toward kt
     uint64_t o_done[2];                  // P.V of tile kt done -> o_done[kt % 2]
     uint64_t recv_full[2];               // local expect_tx + the peer's asynchronous stores (bytes)
-    uint64_t can_send[2];                // arrived by the peer's 4 row warps after reading its recv[b]
+    uint64_t can_send[2];                // arrived by the peer's releaser once the peer has read its recv[b]
+    uint64_t recv_read[2];               // my 4 softmax warps have read recv[b] (local)
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -199,10 +203,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(&s.s_sent[i], 4);
             mbar_init(&s.o_done[i], 1);
         }
-        mbar_init(&s.p_ready, kHeads);
+        for (int i = 0; i < 2; ++i) mbar_init(&s.p_ready[i], kHeads);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.recv_full[i], 1);
-            mbar_init(&s.can_send[i], 4);
+            mbar_init(&s.can_send[i], 1);
+            mbar_init(&s.recv_read[i], 4);
         }
         s.abort = 0;
         fence_mbar_init();
@@ -256,7 +261,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t idesc_o = idesc_f16(kHeads, 256, prm.bf16 != 0, false, true);
             bool ok = (rank != 0 || mbar_wait(&s.q_full, 0)) && mbar_wait(&s.q_ready, 0);
             auto issue_pv = [&](int kt) -> bool {
-                if (!mbar_wait(&s.p_ready, kt & 1)) return false;
+                if (!mbar_wait(&s.p_ready[kt & 1], (kt / 2) & 1)) return false;
                 tc_fence_after();
                 const int st = kt % kStages;
                 const uint32_t v_addr = smem_u32(s.kv[st][0]);
@@ -294,6 +299,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 atomicExch(&s.abort, 1);
                 atomicCAS(prm.status, 0, PA_DEVICE_TIMEOUT_MMA);
             }
+        }
+    } else if (warp == 10) {
+        // -------------------------------------------------------- releaser --
+        // Tells the peer's senders that recv[b] may be overwritten.  The
+        // softmax warps only arrive on a local barrier; the cluster-scope
+        // release (ordered after their reads through this warp's acquire of
+        // that barrier) is paid here, off the softmax path.
+        bool ok = true;
+        const uint32_t can_send_peer0 = peer_addr(smem_u32(&s.can_send[0]), peer);
+        for (int kt = 0; ok && kt < n_kt; ++kt) {
+            const int b = kt & 1;
+            ok = mbar_wait(&s.recv_read[b], (kt / 2) & 1);
+            if (ok && lane == 0) arrive_remote(can_send_peer0 + (uint32_t)b * 8u);
+        }
+        if (!ok) {
+            atomicExch(&s.abort, 1);
+            atomicCAS(prm.status, 0, PA_DEVICE_TIMEOUT_SOFTMAX);
         }
     } else if (warp >= 6) {
         // --------------------------------------------------------- senders --
@@ -338,8 +360,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // softmax, P into TMEM over the S columns (once the senders have read them).
         const int r = tid;
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        const uint32_t can_send_peer0 = peer_addr(smem_u32(&s.can_send[0]), peer);
-        auto can_send_peer = [&](int b) { return can_send_peer0 + (uint32_t)b * 8u; };
         const int sw = r & 15;                   // chunk swizzle of row r
         {
             // latent Q row (this CTA's 256 columns) into TMEM as 16-bit pairs; rows past H are zero
@@ -399,10 +419,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mb = fmax3(mb, cur[c + 2], cur[c + 3]);
             }
             const float mt = fmaxf(ma, mb) * prm.scale_log2;   // the scale is positive
-            // this warp's rows of recv[sb] are read: release them to the peer's
-            // senders (the release orders every lane's reads before the arrive)
+            // this warp's rows of recv[sb] are read (the releaser passes it on)
             __syncwarp();
-            if (lane == 0) arrive_remote(can_send_peer(sb));
+            if (lane == 0) mbar_arrive(&s.recv_read[sb]);
             float alpha = 1.f;
             if (mt > m_ref + kSlack) {
                 alpha = exp2f(m_ref - mt);
@@ -462,7 +481,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();  // the zeroed rows before the tensor core reads them
             }
             tc_fence_before();
-            mbar_arrive(&s.p_ready);
+            mbar_arrive(&s.p_ready[kt & 1]);
         }
         if (ok && n_kt > 0)
             ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) & 1], ((n_kt - 1) / 2) & 1));

@@ -10,13 +10,16 @@
 //   warps 0-7  softmax / O correction / epilogue: query row r (TMEM lane r) is
 //              shared by warps r/32 and r/32+4, each taking 64 of the 128 key
 //              (and output) columns; row maxima and sums cross over shared memory;
-//   warp 8     TMA producer: Q once, then K/V tiles of 128 keys gathered
-//              page by page through the block table (one 16-row box per
-//              page and 64-column half, 128-byte swizzle);
+//   warps 8/10 TMA producers: Q once and K tiles (warp 8), V tiles (warp 10)
+//              of 128 keys gathered page by page through the block table
+//              (one box per page and 64-column half, 128-byte swizzle), each
+//              through its own ring, so K is released once S is computed;
 //   warp 9     MMA issuer: S = Q K^T into one of three TMEM buffers, then
 //              O += P V with P read from tensor memory: the softmax warps
 //              overwrite their row of the S buffer with P as 16-bit pairs.
-// K/V tiles use a 3-stage shared-memory ring; P never touches shared memory.
+// K and V tiles use 3-stage shared-memory rings; P never touches shared memory.
+// CTAs of a cluster (query heads of one KV head, same query tile) receive each
+// K/V tile by multicast: one L2 read feeds all of them.
 // Key tiles past the last query's position are never loaded; the diagonal
 // tiles are masked per row.  Keys at or past the sequence length never reach
 // P.V: their scores are masked and their V rows are zeroed in shared memory
@@ -43,7 +46,7 @@ constexpr int kM = 128;          // queries per tile (TMEM lanes)
 constexpr int kN = 128;          // keys per tile
 constexpr int kD = 128;          // head dim (== value dim)
 constexpr int kStages = 3;
-constexpr int kThreads = 320;        // 8 softmax warps + producer + MMA issuer
+constexpr int kThreads = 352;        // 8 softmax warps + K producer + MMA issuer + V producer
 constexpr uint32_t kHalfBytes = kM * 128;          // one 64-column half of a 128-row tile
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;    // 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
@@ -55,10 +58,14 @@ struct Smem {
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kTileBytes];
     uint64_t q_full;
-    uint64_t kv_full[kStages];
-    uint64_t kv_empty[kStages];
+    uint64_t k_full[kStages];      // K tile landed
+    uint64_t k_empty[kStages];     // S of the tile done in every CTA of the cluster (K free)
+    uint64_t v_full[kStages];
+    uint64_t v_empty[kStages];     // P.V of the tile done in every CTA of the cluster (V free)
     uint64_t s_full[3];            // S of tile kt in TMEM buffer kt % 3
-    uint64_t p_ready;
+    uint64_t p_ready[3];           // P of tile kt in TMEM (all 256 softmax threads) -> p_ready[kt % 3].
+                                   // One barrier per tile in flight: S runs two tiles ahead, so warps
+                                   // can be up to two tiles apart and must not count toward another tile
     uint64_t o_done[3];            // P.V of tile kt done -> o_done[kt % 3]
     float xred[2 * kM];            // row-max / row-sum exchange between the two warps of a row
     uint64_t xa[4], xb[4];         // per lane quarter: values written / values read
@@ -127,11 +134,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         mbar_init(&s.q_full, 1);
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&s.kv_full[i], 1);
-            mbar_init(&s.kv_empty[i], csize);      // one release per CTA of the cluster
+            mbar_init(&s.k_full[i], 1);
+            mbar_init(&s.k_empty[i], csize);       // one release per CTA of the cluster
+            mbar_init(&s.v_full[i], 1);
+            mbar_init(&s.v_empty[i], csize);
         }
         for (int i = 0; i < 3; ++i) mbar_init(&s.s_full[i], 1);
-        mbar_init(&s.p_ready, 2 * kM);
+        for (int i = 0; i < 3; ++i) mbar_init(&s.p_ready[i], 2 * kM);
         for (int i = 0; i < 4; ++i) {
             mbar_init(&s.xa[i], 64);
             mbar_init(&s.xb[i], 64);
@@ -151,30 +160,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tmem_s = [tmem](int b) -> uint32_t { return tmem + 128u * (uint32_t)b; };   // S / P buffers 0..2
     const uint32_t tmem_o = tmem + 384;
 
-    if (warp == 8) {
-        // ---------------------------------------------------- TMA producer --
-        // Lane 0 owns the barriers; lanes 0..pages_per_tile-1 each gather one
-        // page of K and V (4 boxes), so the box issue runs 8 lanes wide.
+    if (warp == 8 || warp == 10) {
+        // ------------------------------------------------- TMA producers --
+        // Warp 8 streams K (and Q once), warp 10 streams V, each through its own
+        // 3-stage ring: a K stage is free as soon as S of its tile is computed,
+        // a V stage only after P.V, so K runs ahead of V.  Lane 0 owns the
+        // barriers; lanes 0..pages_per_tile-1 each gather one page (two
+        // 64-column boxes).  In a cluster, box j of page p is issued by CTA
+        // (2p + j) % csize and multicast to all.
+        const bool is_k = warp == 8;
         const int pages_per_tile = kN / ps;
+        const CUtensorMap *tm = is_k ? &tm_k : &tm_v;
+        uint64_t *full = is_k ? s.k_full : s.v_full;
+        uint64_t *empty = is_k ? s.k_empty : s.v_empty;
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(&s.q_full, kTileBytes);
-            tma_load_3d(s.q, &tm_q, 0, h, q0, &s.q_full);
-            tma_load_3d(s.q + kHalfBytes, &tm_q, 64, h, q0, &s.q_full);
+            tma_prefetch_desc(tm);
+            if (is_k) {
+                tma_prefetch_desc(&tm_q);
+                mbar_arrive_expect_tx(&s.q_full, kTileBytes);
+                tma_load_3d(s.q, &tm_q, 0, h, q0, &s.q_full);
+                tma_load_3d(s.q + kHalfBytes, &tm_q, 64, h, q0, &s.q_full);
+            }
         }
         const int oob_row = prm.plan.pages * ps;          // rows >= this read as zeros
         const int used_pages = (seq_len + ps - 1) / ps;
         for (int kt = 0; kt < n_kt; ++kt) {
             const int st = kt % kStages;
+            uint8_t *ring = is_k ? s.k[st] : s.v[st];
             bool go = true;
             if (lane == 0) {
-                if (kt >= kStages && !mbar_wait(&s.kv_empty[st], ((kt / kStages) - 1) & 1)) {
+                if (kt >= kStages && !mbar_wait(&empty[st], ((kt / kStages) - 1) & 1)) {
                     set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
                     go = false;
                 } else {
-                    mbar_arrive_expect_tx(&s.kv_full[st], 2 * kTileBytes);
+                    mbar_arrive_expect_tx(&full[st], kTileBytes);
                 }
             }
             go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
@@ -183,19 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int lp = (kt0 + kt) * pages_per_tile + lane;
                 const int row = lp < used_pages ? trow[lp] * ps : oob_row;
                 const uint32_t off = (uint32_t)lane * ps * 128;
-                if (csize == 1) {
-                    tma_load_3d(s.k[st] + off, &tm_k, 0, kvh, row, &s.kv_full[st]);
-                    tma_load_3d(s.k[st] + kHalfBytes + off, &tm_k, 64, kvh, row, &s.kv_full[st]);
-                    tma_load_3d(s.v[st] + off, &tm_v, 0, kvh, row, &s.kv_full[st]);
-                    tma_load_3d(s.v[st] + kHalfBytes + off, &tm_v, 64, kvh, row, &s.kv_full[st]);
-                } else {
-                    // boxes K lo, K hi, V lo, V hi of this page: box j is issued by CTA j % csize
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if ((uint32_t)(j % (int)csize) != crank) continue;
-                        uint8_t *dst = (j < 2 ? s.k[st] : s.v[st]) + (j & 1) * kHalfBytes + off;
-                        tma_load_3d_multicast(dst, j < 2 ? &tm_k : &tm_v, (j & 1) * 64, kvh, row, &s.kv_full[st],
-                                              cmask);
+                for (int j = 0; j < 2; ++j) {
+                    if (csize == 1) {
+                        tma_load_3d(ring + j * kHalfBytes + off, tm, j * 64, kvh, row, &full[st]);
+                    } else if ((uint32_t)((2 * lane + j) % (int)csize) == crank) {
+                        tma_load_3d_multicast(ring + j * kHalfBytes + off, tm, j * 64, kvh, row, &full[st], cmask);
                     }
                 }
             }
@@ -204,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // last ones so none lands after this CTA has exited.
         if (csize > 1 && lane == 0) {
             for (int kt = max(0, n_kt - kStages); kt < n_kt; ++kt)
-                if (!mbar_wait(&s.kv_empty[kt % kStages], (kt / kStages) & 1)) {
+                if (!mbar_wait(&empty[kt % kStages], (kt / kStages) & 1)) {
                     set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
                     break;
                 }
@@ -217,7 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t q_addr = smem_u32(s.q);
             bool ok = mbar_wait(&s.q_full, 0);
             auto issue_pv = [&](int kt) -> bool {
-                if (!mbar_wait(&s.p_ready, kt & 1)) return false;
+                if (!mbar_wait(&s.p_ready[kt % 3], (kt / 3) & 1)) return false;
+                if (!mbar_wait(&s.v_full[kt % kStages], (kt / kStages) & 1)) return false;
                 tc_fence_after();
                 const int st = kt % kStages;
                 const uint32_t v_addr = smem_u32(s.v[st]);
@@ -228,15 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&s.o_done[kt % 3]);
                 if (csize == 1)
-                    mma_commit(&s.kv_empty[st]);
+                    mma_commit(&s.v_empty[st]);
                 else
-                    mma_commit_multicast(&s.kv_empty[st], cmask);   // this CTA's copy of the stage is free
+                    mma_commit_multicast(&s.v_empty[st], cmask);   // this CTA's copy of the V stage is free
                 return true;
             };
             // S runs two tiles ahead of P.V: S0, S1, then per tile P.V(kt), S(kt+2).
             auto issue_s = [&](int kt) -> bool {
                 const int st = kt % kStages, sb = kt % 3;
-                if (!mbar_wait(&s.kv_full[st], (kt / kStages) & 1)) return false;
+                if (!mbar_wait(&s.k_full[st], (kt / kStages) & 1)) return false;
                 // the buffer's previous tile (kt-3) must be through its P.V (P lives in it)
                 if (kt >= 3 && !mbar_wait(&s.o_done[sb], ((kt / 3) - 1) & 1)) return false;
                 tc_fence_after();
@@ -247,6 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                smem_desc(k_addr + o, 16, 1024, kLayoutSwizzle128B), idesc_s, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&s.s_full[sb]);
+                if (csize == 1)
+                    mma_commit(&s.k_empty[st]);
+                else
+                    mma_commit_multicast(&s.k_empty[st], cmask);   // this CTA's copy of the K stage is free
                 return true;
             };
             for (int kt = 0; ok && kt < 2 && kt < n_kt; ++kt) ok = issue_s(kt);
@@ -357,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // V rows at or past the sequence end (tail slots) must not reach the MMA
             if ((kt0 + kt) * kN + kN > seq_len) {
                 const int st = kt % kStages;
-                ok = __all_sync(0xffffffffu, mbar_wait(&s.kv_full[st], (kt / kStages) & 1));
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.v_full[st], (kt / kStages) & 1));
                 if (!ok) break;
                 if ((kt0 + kt) * kN + r >= seq_len) {
                     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -368,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();  // the zeroed V rows before the tensor core reads them
             }
             tc_fence_before();
-            mbar_arrive(&s.p_ready);
+            mbar_arrive(&s.p_ready[kt % 3]);
         }
         if (ok && n_kt > 0)
             ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) % 3], ((n_kt - 1) / 3) & 1));

@@ -127,3 +127,52 @@ def test_long_context_window_sampled(cuda_device):
     rows = np.sort(rng.choice(case.num_queries * case.hq, size=24, replace=False))
     _compare(case, window, splits=splits, rows=rows, what="long context")
     _compare(case, window, rows=rows, what="long context unsplit")
+
+
+@pytest.mark.parametrize("ps", [64, 128])
+def test_mla_window_repeatable(cuda_device, ps):
+    """Thirty runs of a windowed MLA layer give the same bits every time.
+
+    A short first window tile sets a low reference maximum, so later tiles
+    rescale O often; the softmax warps then drift apart, which once let a
+    warp already on the next tile complete the current tile's P barrier
+    (seen as NaN in one warp's rows on one CTA of the pair).
+    """
+    seq_lens = [1, 64, 65, 500, 3000]
+    queries = decode_queries(seq_lens) + [(4, 1234)]
+    case = build_case("win_mla_rep", 56, seq_lens, queries, 128, 1, 512, 64, ps, torch.bfloat16,
+                      1 / math.sqrt(192), mla_p=64)
+    dc = case.to("cuda")
+    plan = plan_for(case)
+    pka.paged_kv_store(plan, dc.new_k, dc.new_v, dc.k_cache, dc.v_cache)
+    first = None
+    for _ in range(30):
+        out = pka.paged_mla_forward(plan, dc.q, dc.qp, dc.k_cache, dc.v_cache, case.scale, window=2048)
+        torch.cuda.synchronize()
+        assert pka.device_status() == 0
+        assert torch.isfinite(out.float()).all()
+        if first is None:
+            first = out.clone()
+        else:
+            assert torch.equal(out.view(torch.int16), first.view(torch.int16))
+
+
+def test_prefill_window_repeatable(cuda_device):
+    """The same for prefill tiles, whose softmax warps can be two tiles apart."""
+    seq_lens = [900, 2000]
+    queries = [(0, 400 + i) for i in range(500)] + [(1, 1500 + i) for i in range(500)]
+    case = build_case("win_pf_rep", 57, seq_lens, queries, 32, 8, 128, 128, 16, torch.bfloat16,
+                      1 / math.sqrt(128))
+    dc = case.to("cuda")
+    plan = plan_for(case)
+    pka.paged_kv_store(plan, dc.new_k, dc.new_v, dc.k_cache, dc.v_cache)
+    first = None
+    for _ in range(30):
+        out = pka.paged_attn_forward(plan, dc.q, dc.k_cache, dc.v_cache, case.scale, window=37)
+        torch.cuda.synchronize()
+        assert pka.device_status() == 0
+        assert torch.isfinite(out.float()).all()
+        if first is None:
+            first = out.clone()
+        else:
+            assert torch.equal(out.view(torch.int16), first.view(torch.int16))
