@@ -312,6 +312,7 @@ pa_status pa_time_next_kernel(void *start_event, void *stop_event);
 #define PA_DEVICE_TIMEOUT_MMA 2
 #define PA_DEVICE_TIMEOUT_SOFTMAX 3
 #define PA_DEVICE_RANGE 4
+#define PA_DEVICE_LAYOUT 5   /* a kernel found its shared memory misplaced and did nothing */
 pa_status pa_device_status(int32_t *code, int32_t clear);
 
 #ifdef __cplusplus

@@ -67,13 +67,19 @@ struct Smem {
                                    // One barrier per tile in flight: S runs two tiles ahead, so warps
                                    // can be up to two tiles apart and must not count toward another tile
     uint64_t o_done[3];            // P.V of tile kt done -> o_done[kt % 3]
-    float xred[2 * kM];            // row-max / row-sum exchange between the two warps of a row
-    uint64_t xa[4], xb[4];         // per lane quarter: values written / values read
+    float xred[2][2 * kM];         // row-max / row-sum exchange between the two warps of a row,
+                                   // slot n % 2 for exchange n
+    uint64_t xa[2][4];             // per slot and lane quarter: both warps' values written
     uint32_t tmem_base;
     int32_t abort;
 };
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+// The operand tiles need 1024-byte alignment (128-byte swizzle atoms); the
+// dynamic shared memory is declared with that alignment, so no slack is
+// requested (the struct fills the 227 KB a block may have).  The kernel checks
+// the alignment and refuses to run (PA_DEVICE_LAYOUT) if it ever differs.
+constexpr size_t kSmemBytes = sizeof(Smem);
+static_assert(kSmemBytes <= 232448, "prefill shared memory above the per-block limit");
 
 struct PrefillParams {
     PlanView plan;
@@ -105,8 +111,12 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, PrefillParams prm) {
-    extern __shared__ uint8_t smem_raw[];
-    Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if ((smem_u32(smem_raw) & 1023u) != 0u) {
+        if (threadIdx.x == 0) atomicCAS(prm.status, 0, PA_DEVICE_LAYOUT);
+        return;
+    }
+    Smem &s = *reinterpret_cast<Smem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // Heaviest tiles first: the plan orders tiles by decreasing key count.
@@ -142,8 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 3; ++i) mbar_init(&s.s_full[i], 1);
         for (int i = 0; i < 3; ++i) mbar_init(&s.p_ready[i], 2 * kM);
         for (int i = 0; i < 4; ++i) {
-            mbar_init(&s.xa[i], 64);
-            mbar_init(&s.xb[i], 64);
+            mbar_init(&s.xa[0][i], 64);
+            mbar_init(&s.xa[1][i], 64);
         }
         for (int i = 0; i < 3; ++i) mbar_init(&s.o_done[i], 1);
         s.abort = 0;
@@ -288,13 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int xphase = 0;
         // value of the other warp of this row (bounded waits; false on timeout)
+        // One barrier round per exchange: slot n % 2 is written again at exchange
+        // n + 2 only after the partner arrived for exchange n + 1, which it does
+        // after reading exchange n.
         auto exchange = [&](float v, float &other) -> bool {
-            if (xphase > 0 && !__all_sync(0xffffffffu, mbar_wait(&s.xb[q4], (xphase - 1) & 1))) return false;
-            s.xred[h2 * kM + r] = v;
-            mbar_arrive(&s.xa[q4]);
-            if (!__all_sync(0xffffffffu, mbar_wait(&s.xa[q4], xphase & 1))) return false;
-            other = s.xred[(1 - h2) * kM + r];
-            mbar_arrive(&s.xb[q4]);
+            const int slot = xphase & 1;
+            s.xred[slot][h2 * kM + r] = v;
+            mbar_arrive(&s.xa[slot][q4]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.xa[slot][q4], (xphase >> 1) & 1))) return false;
+            other = s.xred[slot][(1 - h2) * kM + r];
             ++xphase;
             return true;
         };
@@ -363,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 16; ++i) {
                     const float2 x = ffma2(make_float2(__uint_as_float(sv[c + 2 * i]), __uint_as_float(sv[c + 2 * i + 1])),
                                            sc2, nm2);
-                    const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                    // 3 pairs in 8 on the FMA pipe, the rest on the special-function unit
+                    const float2 pp = (i % 8 >= 5) ? exp2_poly2(x) : make_float2(ex2(x.x), ex2(x.y));
                     ls2 = fadd2(ls2, pp);
                     pk[i] = pack2<T>(pp.x, pp.y);
                 }
