@@ -54,18 +54,19 @@ def visible_counts(case) -> np.ndarray:
     return case.seq_lens[case.query_seq].astype(np.int64)
 
 
-def kv_bytes(case) -> int:
-    """Algorithmic K/V bytes: each query's visible keys, each KV head read once."""
+def kv_bytes(case, first: int = 0) -> int:
+    """Algorithmic K/V bytes: each query's visible keys (queries first.. on), each KV head read once."""
     elt = torch.empty((), dtype=case.dtype).element_size()
-    n = int(visible_counts(case).sum())
+    n = int(visible_counts(case)[first:].sum())
     if case.is_mla:
         return n * (case.d + case.p) * elt
     return n * case.hkv * (case.d + case.dv) * elt
 
 
-def attn_flops(case) -> int:
-    """Multiply-add flops over causal-visible (query, key) pairs."""
-    n = int(visible_counts(case).sum())
+def attn_flops(case, first: int = 0, count: int | None = None) -> int:
+    """Multiply-add flops over causal-visible (query, key) pairs (of queries first..first+count-1)."""
+    vc = visible_counts(case)
+    n = int(vc[first:None if count is None else first + count].sum())
     if case.is_mla:
         return n * case.hq * (2 * (case.d + case.p) + 2 * case.d)
     return n * case.hq * (2 * case.d + 2 * case.dv)
@@ -336,11 +337,29 @@ def secondary(device, warmup: int, steps: int, peaks, which):
         e1.record()
         torch.cuda.synchronize(device)
         ms = e0.elapsed_time(e1) / steps
+        # the call's main kernel alone (prefill tiles / MLA), events recorded by the library
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            st.pka.time_next_kernel(*kev[i])
+            st.attend()
+        torch.cuda.synchronize(device)
+        kms = sum(a.elapsed_time(b) for a, b in kev) / steps
         fl = attn_flops(case)
         res[name] = {"queries": case.num_queries, "splits": st.splits, "ms": ms, "flops": fl,
                      "tflops": fl / ms / 1e9, "frac_bf16_peak": fl / ms / 1e9 / tc,
-                     "kv_gbs": kv_bytes(case) / ms / 1e6, "frac_hbm": kv_bytes(case) / ms / 1e6 / hbm,
                      "prefill_tiles": st.plan.n_tiles, "decode_items": st.plan.n_decode}
+        if case.is_mla:
+            res[name].update(kernel_ms=kms, kernel_tflops=fl / kms / 1e9, kernel_frac_bf16_peak=fl / kms / 1e9 / tc,
+                             kv_gbs=kv_bytes(case) / ms / 1e6, frac_hbm=kv_bytes(case) / ms / 1e6 / hbm)
+        else:
+            # prefill chunks are the first n_prefill * chunk queries; their kernel is timed alone
+            # (the call then runs the decode items, an HBM-bound kernel, after it)
+            npq = case.meta["n_prefill"] * case.meta["chunk"]
+            pfl = attn_flops(case, 0, npq)
+            res[name].update(prefill_kernel_ms=kms, prefill_flops=pfl, prefill_kernel_tflops=pfl / kms / 1e9,
+                             prefill_kernel_frac_bf16_peak=pfl / kms / 1e9 / tc,
+                             decode_kv_bytes=kv_bytes(case, npq), note="ms and tflops cover the whole call: the "
+                             "prefill kernel, then the decode items (HBM-bound)")
         del st, case
         torch.cuda.empty_cache()
     return res

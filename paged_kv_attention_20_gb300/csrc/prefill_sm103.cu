@@ -475,10 +475,10 @@ cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {
     prm.causal = a.causal;
     prm.window = a.window;
     prm.bf16 = bf16 ? 1 : 0;
-    // Cluster of up to 4 CTAs = query heads sharing one KV head (consecutive
+    // Cluster of 2 CTAs = query heads sharing one KV head (consecutive
     // blocks: block = tile * Hq + head, and the group size divides Hq).
     const int group = a.hq / a.hkv;
-    const unsigned csize = group % 4 == 0 ? 4u : group % 2 == 0 ? 2u : 1u;
+    const unsigned csize = group % 2 == 0 ? 2u : 1u;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(a.plan.n_tiles * a.hq));
     cfg.blockDim = dim3(kThreads);
