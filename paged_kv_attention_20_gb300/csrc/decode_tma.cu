@@ -3,9 +3,10 @@
 // Same operation as decode.cu (ruDNN 0.1.7, src/paged_attention/mod.rs:
 // `DevicePlan::attention`, `execute_attention_into`, `attention_into_split`),
 // organised for GB300's HBM3e:
-//  * one CTA of 4 warps per (query, KV head, group of up to 8 query heads,
-//    split); the GQA heads of one KV head share the CTA, so every page row is
-//    read from HBM once;
+//  * one CTA of 4 warps per (query, KV head, group of up to 4 query heads,
+//    split); the GQA heads of one KV head share the CTA (larger groups use
+//    adjacent CTAs, whose second read of a page hits L2), so every page row
+//    is read from HBM once;
 //  * the split's keys are cut into 16-token tiles; warp w owns tiles w, w+4,
 //    w+8, ... and runs its own online softmax over them, with no CTA-wide
 //    barrier in the loop; the four warp states are merged once at the end;
@@ -409,8 +410,11 @@ cudaError_t launch_t(const AttnArgs &a, int items, int use_list, const CUtensorM
 template <typename T, int D>
 cudaError_t launch_d(const AttnArgs &a, int items, int use_list, const CUtensorMap &tk, const CUtensorMap &tv,
                      const TmaParams &tp, cudaStream_t st) {
+    // At most 4 query heads per CTA: larger groups are covered by several CTAs
+    // per KV head (adjacent blocks, so the second read of a page hits L2).  With
+    // 8 heads in one CTA the kernel is issue-bound (about 8 flop per KV byte on
+    // CUDA cores, twice the registers); two CTAs of 4 measured faster.
     const int G = a.hq / a.hkv;
-    if (G % 8 == 0) return launch_t<T, D, 8>(a, items, use_list, tk, tv, tp, st);
     if (G % 4 == 0) return launch_t<T, D, 4>(a, items, use_list, tk, tv, tp, st);
     if (G % 2 == 0) return launch_t<T, D, 2>(a, items, use_list, tk, tv, tp, st);
     return launch_t<T, D, 1>(a, items, use_list, tk, tv, tp, st);
