@@ -14,9 +14,11 @@
 //              of 128 keys gathered page by page through the block table
 //              (one box per page and 64-column half, 128-byte swizzle), each
 //              through its own ring, so K is released once S is computed;
-//   warp 9     MMA issuer: S = Q K^T into one of three TMEM buffers, then
-//              O += P V with P read from tensor memory: the softmax warps
-//              overwrite their row of the S buffer with P as 16-bit pairs.
+//   warps 9/11 MMA issuers: warp 9 issues S = Q K^T into one of three TMEM
+//              buffers, warp 11 issues O += P V with P read from tensor memory
+//              (the softmax warps overwrite their row of the S buffer with P as
+//              16-bit pairs); two issuers, because the tensor core takes only a
+//              few MMAs ahead and one thread blocked on S noticed P late.
 // K and V tiles use 3-stage shared-memory rings; P never touches shared memory.
 // CTAs of a cluster (query heads of one KV head, same query tile) receive each
 // K/V tile by multicast: one L2 read feeds all of them.
@@ -46,7 +48,7 @@ constexpr int kM = 128;          // queries per tile (TMEM lanes)
 constexpr int kN = 128;          // keys per tile
 constexpr int kD = 128;          // head dim (== value dim)
 constexpr int kStages = 3;
-constexpr int kThreads = 352;        // 8 softmax warps + K producer + MMA issuer + V producer
+constexpr int kThreads = 384;        // 8 softmax warps + K producer + S issuer + V producer + P.V issuer
 constexpr uint32_t kHalfBytes = kM * 128;          // one 64-column half of a 128-row tile
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;    // 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
@@ -231,55 +233,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
         }
-    } else if (warp == 9) {
-        // ------------------------------------------------------ MMA issuer --
+    } else if (warp == 9 || warp == 11) {
+        // ------------------------------------------------------ MMA issuers --
+        // Two issuing threads: warp 9 issues S = Q K^T (three TMEM buffers, so
+        // S runs up to two tiles ahead of P.V), warp 11 issues O += P V as soon
+        // as P of a tile is in TMEM.  The tensor core accepts only a few MMAs
+        // ahead, so a single issuer spends most of a tile blocked on one kind
+        // and notices the other late.  The two touch different TMEM (S buffers
+        // vs O) and shared memory (K vs V), and each commits its own MMAs.
         if (lane == 0) {
-            const uint32_t idesc_s = idesc_f16(kM, kN, prm.bf16 != 0, false, false);
-            const uint32_t idesc_o = idesc_f16(kM, kD, prm.bf16 != 0, false, true);
-            const uint32_t q_addr = smem_u32(s.q);
-            bool ok = mbar_wait(&s.q_full, 0);
-            auto issue_pv = [&](int kt) -> bool {
-                if (!mbar_wait(&s.p_ready[kt % 3], (kt / 3) & 1)) return false;
-                if (!mbar_wait(&s.v_full[kt % kStages], (kt / kStages) & 1)) return false;
-                tc_fence_after();
-                const int st = kt % kStages;
-                const uint32_t v_addr = smem_u32(s.v[st]);
-                const uint32_t p_tmem = tmem_s(kt % 3);          // P (16-bit pairs) over the S columns
-                for (int ks = 0; ks < kN / 16; ++ks) {
-                    const uint64_t b = smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, kLayoutSwizzle128B);
-                    mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
+            bool ok = true;
+            if (warp == 9) {
+                const uint32_t idesc_s = idesc_f16(kM, kN, prm.bf16 != 0, false, false);
+                const uint32_t q_addr = smem_u32(s.q);
+                ok = mbar_wait(&s.q_full, 0);
+                for (int kt = 0; ok && kt < n_kt; ++kt) {
+                    const int st = kt % kStages, sb = kt % 3;
+                    if (!mbar_wait(&s.k_full[st], (kt / kStages) & 1)) { ok = false; break; }
+                    // the buffer's previous tile (kt-3) must be through its P.V (P lives in it)
+                    if (kt >= 3 && !mbar_wait(&s.o_done[sb], ((kt / 3) - 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t k_addr = smem_u32(s.k[st]);
+                    for (int ks = 0; ks < kD / 16; ++ks) {
+                        const uint32_t o = (ks / 4) * kHalfBytes + (ks % 4) * 32;
+                        mma_f16_ss(tmem_s(sb), smem_desc(q_addr + o, 16, 1024, kLayoutSwizzle128B),
+                                   smem_desc(k_addr + o, 16, 1024, kLayoutSwizzle128B), idesc_s, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&s.s_full[sb]);
+                    if (csize == 1)
+                        mma_commit(&s.k_empty[st]);
+                    else
+                        mma_commit_multicast(&s.k_empty[st], cmask);   // this CTA's copy of the K stage is free
                 }
-                mma_commit(&s.o_done[kt % 3]);
-                if (csize == 1)
-                    mma_commit(&s.v_empty[st]);
-                else
-                    mma_commit_multicast(&s.v_empty[st], cmask);   // this CTA's copy of the V stage is free
-                return true;
-            };
-            // S runs two tiles ahead of P.V: S0, S1, then per tile P.V(kt), S(kt+2).
-            auto issue_s = [&](int kt) -> bool {
-                const int st = kt % kStages, sb = kt % 3;
-                if (!mbar_wait(&s.k_full[st], (kt / kStages) & 1)) return false;
-                // the buffer's previous tile (kt-3) must be through its P.V (P lives in it)
-                if (kt >= 3 && !mbar_wait(&s.o_done[sb], ((kt / 3) - 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t k_addr = smem_u32(s.k[st]);
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t o = (ks / 4) * kHalfBytes + (ks % 4) * 32;
-                    mma_f16_ss(tmem_s(sb), smem_desc(q_addr + o, 16, 1024, kLayoutSwizzle128B),
-                               smem_desc(k_addr + o, 16, 1024, kLayoutSwizzle128B), idesc_s, ks > 0 ? 1u : 0u);
+            } else {
+                const uint32_t idesc_o = idesc_f16(kM, kD, prm.bf16 != 0, false, true);
+                for (int kt = 0; ok && kt < n_kt; ++kt) {
+                    const int st = kt % kStages;
+                    if (!mbar_wait(&s.p_ready[kt % 3], (kt / 3) & 1)) { ok = false; break; }
+                    if (!mbar_wait(&s.v_full[st], (kt / kStages) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t v_addr = smem_u32(s.v[st]);
+                    const uint32_t p_tmem = tmem_s(kt % 3);          // P (16-bit pairs) over the S columns
+                    for (int ks = 0; ks < kN / 16; ++ks) {
+                        const uint64_t b = smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, kLayoutSwizzle128B);
+                        mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&s.o_done[kt % 3]);
+                    if (csize == 1)
+                        mma_commit(&s.v_empty[st]);
+                    else
+                        mma_commit_multicast(&s.v_empty[st], cmask);   // this CTA's copy of the V stage is free
                 }
-                mma_commit(&s.s_full[sb]);
-                if (csize == 1)
-                    mma_commit(&s.k_empty[st]);
-                else
-                    mma_commit_multicast(&s.k_empty[st], cmask);   // this CTA's copy of the K stage is free
-                return true;
-            };
-            for (int kt = 0; ok && kt < 2 && kt < n_kt; ++kt) ok = issue_s(kt);
-            for (int kt = 0; ok && kt < n_kt; ++kt) {
-                ok = issue_pv(kt);
-                if (ok && kt + 2 < n_kt) ok = issue_s(kt + 2);
             }
             if (!ok) set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_MMA);
         }
