@@ -379,8 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 16; ++i) {
                     const float2 x = ffma2(make_float2(__uint_as_float(sv[c + 2 * i]), __uint_as_float(sv[c + 2 * i + 1])),
                                            sc2, nm2);
-                    // 3 pairs in 8 on the FMA pipe, the rest on the special-function unit
-                    const float2 pp = (i % 8 >= 5) ? exp2_poly2(x) : make_float2(ex2(x.x), ex2(x.y));
+                    const float2 pp = make_float2(ex2(x.x), ex2(x.y));
                     ls2 = fadd2(ls2, pp);
                     pk[i] = pack2<T>(pp.x, pp.y);
                 }

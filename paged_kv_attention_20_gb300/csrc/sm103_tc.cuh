@@ -43,17 +43,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking test: has the phase with the given parity completed?
-__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // try_wait that lets the hardware suspend the thread for up to `hint_ns`
 // before reporting "not yet" (the thread resumes as soon as the phase completes).
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
@@ -274,32 +263,6 @@ __device__ __forceinline__ float ex2(float x) {
     float r;
     asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
     return r;
-}
-
-// 2^x for a pair on the FMA and integer pipes, to take part of a softmax's
-// exponentials off the special-function unit.  Range reduction by rounding to
-// the nearest integer (Cody & Waite): x = n + f, f in [-1/2, 1/2]; 2^f from a
-// degree-3 polynomial whose coefficients were fitted for this library by
-// weighted least squares on [-1/2, 1/2] (max relative error 7.5e-5 in fp32,
-// far below the 2^-9 of the 16-bit P it feeds); 2^n is added to the exponent
-// field.  Inputs are clamped to >= -125 so the result stays a normal number:
-// a softmax weight below 2^-125 (0 for the hardware unit) is immaterial next
-// to the row sum, which holds the maximum's weight 1.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    x.x = fmaxf(x.x, -125.f);
-    x.y = fmaxf(x.y, -125.f);
-    const float2 shift = make_float2(12582912.f, 12582912.f);          // 1.5 * 2^23
-    const float2 t = fadd2(x, shift);                                  // round(x) in the low mantissa bits
-    const float2 n = fadd2(t, make_float2(-12582912.f, -12582912.f));  // round(x), exact
-    const float2 f = ffma2(n, make_float2(-1.f, -1.f), x);             // x - round(x), exact
-    float2 p = ffma2(f, make_float2(0.0551716573536396f, 0.0551716573536396f),
-                     make_float2(0.2426111400127411f, 0.2426111400127411f));
-    p = ffma2(p, f, make_float2(0.6932609677314758f, 0.6932609677314758f));
-    p = ffma2(p, f, make_float2(0.9999280571937561f, 0.9999280571937561f));
-    // the bits of t are those of the shift plus round(x); shifted left by 23
-    // only round(x) remains (the shift's low 9 bits are zero), in the exponent field
-    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
 }
 
 // ------------------------------------------------------------- descriptors --
