@@ -144,7 +144,9 @@ size_t pa_workspace_bytes(int32_t queries, int32_t heads, int32_t value_dim, int
  * Split count for paged_attn_forward_split / paged_mla_forward on this plan
  * (libmir-cuda 0.1.0, src/backend/attention/graph/mod.rs enables a split
  * path above a `split_threshold`; its value is not given, this rule is ours):
- * enough (item, kv head, split) blocks to give every SM about four, no split
+ * enough blocks (decode: per item, KV head and group of up to 4 query heads;
+ * prefill: per tile and query head) per split to give every SM about four
+ * (eight when one split has fewer blocks than there are SMs), no split
  * shorter than 4 pages of the longest visible history (at most `window` keys
  * when window > 0), 1..PA_MAX_SPLITS.
  */
@@ -224,12 +226,13 @@ pa_status paged_attn_forward(const pa_plan *plan, const void *q, const void *k_c
 
 /*
  * Split-KV form (`attention_into_split`): the visible history [lo, hi) of
- * every decode query is cut into `splits` contiguous ranges (base = lo rounded
- * down to a page boundary, chunk = ceil((hi - base) / splits) rounded up to a
- * multiple of page_size, split s covers [max(lo, base + s*chunk),
- * min(base + (s+1)*chunk, hi)); lo = 0 without a window); each range writes its normalised fp32
- * partial output and natural-log log-sum-exp into `workspace`, then a merge
- * kernel writes out.  Prefill tiles are computed unsplit.  The workspace
+ * every query -- decode items and each row of a prefill tile alike -- is cut
+ * into `splits` contiguous ranges (base = lo rounded down to a page boundary,
+ * chunk = ceil((hi - base) / splits) rounded up to a multiple of page_size,
+ * split s covers [max(lo, base + s*chunk), min(base + (s+1)*chunk, hi));
+ * lo = 0 without a window); each range writes its normalised fp32 partial
+ * output and natural-log log-sum-exp into `workspace`, then a merge kernel
+ * writes out.  The workspace
  * (>= pa_workspace_bytes(queries, num_heads, value_dim, splits), 16-byte
  * aligned) may be reused by later calls on the same stream with any plan;
  * calls on different streams need different workspaces.  splits == 1 is

@@ -68,10 +68,17 @@ __host__ __device__ inline void visible_range(int pos, int seq_len, int causal, 
 // Every split but the first starts on a page boundary; an empty split has j0 == j1.
 __host__ __device__ inline void split_bounds(int64_t lo, int64_t hi, int splits, int s, int ps, int64_t &j0,
                                              int64_t &j1) {
-    const int64_t base = lo / ps * ps;
-    int64_t n = hi - base;
+    if (splits == 1) {           // the whole range (what the rule below gives for one split)
+        j0 = lo;
+        j1 = hi > lo ? hi : lo;
+        return;
+    }
+    // positions fit 32 bits (the plan checks slots against 2^31), so 32-bit division
+    const int lo32 = (int)lo, hi32 = (int)hi;
+    const int base = lo32 / ps * ps;
+    int n = hi32 - base;
     if (n < 0) n = 0;
-    int64_t chunk = (n + splits - 1) / splits;
+    int chunk = (n + splits - 1) / splits;
     chunk = (chunk + ps - 1) / ps * ps;
     int64_t b = base + (int64_t)s * chunk, e = b + chunk;
     if (b < lo) b = lo;

@@ -275,11 +275,14 @@ size_t pa_workspace_bytes(int32_t queries, int32_t heads, int32_t value_dim, int
 int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t num_kv_heads,
                                    int32_t window, int32_t num_sms) {
     if (!plan || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads || num_sms < 1) return 1;
-    int64_t items = plan->n_decode;
-    if (items == 0) return 1;
+    if (plan->n_decode + plan->n_tiles == 0) return 1;
     int64_t group = num_heads / num_kv_heads;
-    int64_t blocks = items * num_kv_heads * ((group + 7) / 8);
-    int64_t target = 4 * (int64_t)num_sms;
+    // decode CTAs (one per KV head and group of up to 4 query heads) plus the
+    // prefill CTAs (one per tile and query head), per split
+    int64_t blocks = (int64_t)plan->n_decode * num_kv_heads * ((group + 3) / 4) + (int64_t)plan->n_tiles * num_heads;
+    // about four blocks per SM; a few long histories (fewer blocks than SMs)
+    // get about eight, so the uneven split lengths still balance
+    int64_t target = (blocks >= num_sms ? 4 : 8) * (int64_t)num_sms;
     int64_t s = (target + blocks - 1) / blocks;
     const int64_t longest = window > 0 ? std::min<int64_t>(plan->max_seq_len, window) : plan->max_seq_len;
     int64_t cap = std::max<int64_t>(1, longest / (4 * (int64_t)plan->page_size));
@@ -393,13 +396,12 @@ pa_status attention(const pa_plan *plan, const void *q, const void *k, const voi
     } else {
         bool tiles = plan->n_tiles > 0 && pa::prefill_supported(a);
         if (tiles) {
+            // with splits > 1 both kernels write partials and one merge covers every query
             mark(t0);
             e = pa::launch_prefill(a, st);
             mark(t1);
-            if (e == cudaSuccess && plan->n_decode > 0) {
-                e = pa::launch_decode(a, true, st);
-                if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, true, st);
-            }
+            if (e == cudaSuccess && plan->n_decode > 0) e = pa::launch_decode(a, true, st);
+            if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, false, st);
         } else {
             // every query is a decode item: use the (longest-first) decode list
             const bool all_decode = plan->n_tiles == 0;

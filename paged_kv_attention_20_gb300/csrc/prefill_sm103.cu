@@ -86,11 +86,13 @@ static_assert(kSmemBytes <= 232448, "prefill shared memory above the per-block l
 struct PrefillParams {
     PlanView plan;
     void *out;
+    float *ws_o, *ws_lse;   // split partials (splits > 1): [S, Q, Hq, 128] and [S, Q, Hq]
     int32_t *status;
     int hq, hkv;
     float scale_log2;
     int causal;
     int window;
+    int splits;
     int bf16;
 };
 
@@ -122,7 +124,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // Heaviest tiles first: the plan orders tiles by decreasing key count.
-    const int tile_idx = blockIdx.x / prm.hq;
+    // block = (tile * splits + split) * Hq + head
+    const int tile_idx = blockIdx.x / (prm.hq * prm.splits);
+    const int split = (blockIdx.x / prm.hq) % prm.splits;
     const int h = blockIdx.x % prm.hq;
     const int kvh = h / (prm.hq / prm.hkv);
     const int4 tile = prm.plan.tiles[tile_idx];
@@ -130,12 +134,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ps = prm.plan.page_size;
     const int seq_len = prm.plan.seq_lens[seq];
     const int last_pos = pos0 + nq - 1;
-    const int n_keys = prm.causal ? last_pos + 1 : seq_len;
-    // Key tiles kt0 .. kt0 + n_kt - 1; under a sliding window the tile's first
-    // query (the lowest position) sees keys from pos0 - window + 1 on.
-    const int lo0 = prm.window > 0 ? max(0, pos0 - prm.window + 1) : 0;
-    const int kt0 = lo0 / kN;
-    const int n_kt = max(0, (n_keys + kN - 1) / kN - kt0);
+    // Keys of row r for this split: its visible range [lo, hi) (causal end,
+    // sliding window) cut by the split partition.  Both ends grow with the
+    // row's position, so the tile's key range runs from the first row's lower
+    // end to the last row's upper end: key tiles kt0 .. kt0 + n_kt - 1.
+    auto row_keys = [&](int pos, int64_t &j0, int64_t &j1) {
+        int64_t lo, hi;
+        visible_range(pos, seq_len, prm.causal, prm.window, lo, hi);
+        split_bounds(lo, hi, prm.splits, split, ps, j0, j1);
+    };
+    int64_t first_j0, first_j1, last_j0, last_j1;
+    row_keys(pos0, first_j0, first_j1);
+    row_keys(last_pos, last_j0, last_j1);
+    const int kt0 = (int)(first_j0 / kN);
+    const int n_kt = last_j1 > first_j0 ? (int)((last_j1 + kN - 1) / kN) - kt0 : 0;
     const int32_t *trow = prm.plan.table + (int64_t)seq * prm.plan.width;
     // CTAs of one cluster hold query heads of the same KV head and the same
     // query tile: they walk the same key tiles, and each K/V tile is loaded once
@@ -296,8 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col0 = 64 * h2;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         const int my_pos = pos0 + r;
-        const int vis_end = prm.causal ? min(my_pos + 1, seq_len) : seq_len;  // keys [vis_lo, vis_end)
-        const int vis_lo = prm.window > 0 ? max(0, my_pos - prm.window + 1) : 0;
+        int64_t row_j0 = 0, row_j1 = 0;           // this row's keys in this split: [vis_lo, vis_end)
+        if (r < nq) row_keys(my_pos, row_j0, row_j1);   // rows past the tile's queries see nothing
+        const int vis_lo = (int)row_j0, vis_end = (int)row_j1;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         int xphase = 0;
@@ -410,10 +423,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) {
             set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_SOFTMAX);
         } else {
-            // every lane loads (warp-collective); only rows of real queries store
+            // every lane loads (warp-collective); only rows of real queries store.
+            // A row with no key in this split (only with splits > 1) writes a zero
+            // partial and lse = -inf; O was not written for it.
             tc_fence_after();
-            const float inv = 1.f / (l + l_other);
-            T *dst = static_cast<T *>(prm.out) + ((int64_t)(q0 + r) * prm.hq + h) * kD + col0;
+            const float lsum = l + l_other;
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            const int64_t orow = (int64_t)(q0 + r) * prm.hq + h;
+            if (prm.splits > 1) {
+                const int64_t rows = (int64_t)prm.plan.queries * prm.hq;
+                float *dst = prm.ws_o + ((int64_t)split * rows + orow) * kD + col0;
+#pragma unroll 1
+                for (int c = 0; c < 64; c += 16) {
+                    uint32_t v[16];
+                    if (n_kt > 0) {
+                        tmem_ld16(tmem_o + lane_off + col0 + c, v);
+                        tmem_wait_ld();
+                    }
+                    if (r < nq) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4 *>(dst + c + i) =
+                                lsum > 0.f ? make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
+                                                         __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                if (r < nq && h2 == 0)
+                    prm.ws_lse[(int64_t)split * rows + orow] =
+                        lsum > 0.f ? (m_ref + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+            } else {
+            T *dst = static_cast<T *>(prm.out) + orow * kD + col0;
 #pragma unroll 1
             for (int c = 0; c < 64; c += 16) {
                 uint32_t v[16];
@@ -432,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     reinterpret_cast<uint4 *>(dst + c)[0] = w0;
                     reinterpret_cast<uint4 *>(dst + c)[1] = w1;
                 }
+            }
             }
         }
     }
@@ -471,6 +512,9 @@ cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {
     PrefillParams prm{};
     prm.plan = a.plan;
     prm.out = a.out;
+    prm.ws_o = a.ws_o;
+    prm.ws_lse = a.ws_lse;
+    prm.splits = a.splits;
     prm.status = a.status;
     prm.hq = a.hq;
     prm.hkv = a.hkv;
@@ -483,7 +527,7 @@ cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {
     const int group = a.hq / a.hkv;
     const unsigned csize = group % 2 == 0 ? 2u : 1u;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(a.plan.n_tiles * a.hq));
+    cfg.gridDim = dim3((unsigned)(a.plan.n_tiles * a.splits * a.hq));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = st;
