@@ -155,10 +155,11 @@ int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32
 
 /*
  * Split count for paged_mla_forward (same source as above; the rule is ours):
- * the tensor-core MLA kernel runs one CTA pair per (query, 128 heads, split);
- * aim for about two waves over `num_sms` SMs, each split keeping at least 256
- * keys of the longest history (at most `window` keys when window > 0),
- * 1..PA_MAX_SPLITS.
+ * the tensor-core MLA kernel runs one CTA pair per (query, 128 heads, split)
+ * and is bound by the tensor pipe, so it splits only as far as needed to give
+ * each of the num_sms / 2 SM pairs work, and to keep the longest history
+ * (pos + 1 keys, at most `window` when window > 0) within 1.25x one pair's
+ * share of all keys; each split keeps at least 256 keys, 1..PA_MAX_SPLITS.
  */
 int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t window, int32_t num_sms);
 

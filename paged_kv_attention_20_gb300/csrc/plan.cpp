@@ -293,13 +293,23 @@ int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32
 
 int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t window, int32_t num_sms) {
     if (!plan || num_heads < 1 || num_sms < 1 || plan->queries == 0) return 1;
-    // one CTA pair per (query, 128 heads, split); aim for about two waves of SMs
-    const int64_t pairs = (int64_t)plan->queries * ((num_heads + 127) / 128);
-    int64_t s = (2 * (int64_t)num_sms + 2 * pairs - 1) / (2 * pairs);
-    int64_t longest = 0;
-    for (int32_t q = 0; q < plan->queries; ++q)
-        longest = std::max<int64_t>(longest, (int64_t)plan->words[plan->off_qmeta + 4 * (size_t)q + 1] + 1);
-    if (window > 0) longest = std::min<int64_t>(longest, window);
+    // One CTA pair per (query, 128 heads, split), one pair per two SMs; the
+    // kernel is tensor-bound, so splits only pay for themselves when pairs
+    // would sit idle or one history dwarfs a pair's share of the work (every
+    // split adds fp32 partials and a merge).
+    const int64_t blocks = (num_heads + 127) / 128;
+    const int64_t pairs = (int64_t)plan->queries * blocks;
+    const int64_t slots = std::max<int64_t>(1, num_sms / 2);
+    int64_t longest = 0, total = 0;
+    for (int32_t q = 0; q < plan->queries; ++q) {
+        int64_t n = (int64_t)plan->words[plan->off_qmeta + 4 * (size_t)q + 1] + 1;
+        if (window > 0) n = std::min<int64_t>(n, window);
+        longest = std::max(longest, n);
+        total += n * blocks;
+    }
+    int64_t s = (slots + pairs - 1) / pairs;                     // every pair slot gets work
+    const double share = 1.25 * (double)total / (double)slots;  // a pair slot's load, with slack
+    if ((double)longest > share) s = std::max<int64_t>(s, (int64_t)std::ceil((double)longest / share));
     const int64_t cap = std::max<int64_t>(1, longest / 256);   // splits of at least 4 tiles of 64 keys
     s = std::max<int64_t>(1, std::min<int64_t>(std::min(s, cap), PA_MAX_SPLITS));
     return (int32_t)s;

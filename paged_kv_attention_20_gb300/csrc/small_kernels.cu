@@ -73,53 +73,110 @@ template <> __device__ __forceinline__ float from_float<float>(float x) { return
 template <> __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
 template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-// grid (items, Hq), 128 threads over the value dim.
-template <typename T>
-__global__ void __launch_bounds__(128) merge_kernel(AttnArgs a, int use_list) {
-    const int item = blockIdx.x, h = blockIdx.y;
+// One warp per (query, head) row, eight rows per 256-thread block.  Every
+// lane derives the split weights e^(lse_s - M) itself (M = max over splits,
+// empty splits weigh 0) and holds VEC consecutive value columns of each
+// 32*VEC-column chunk, read as one vector per split.
+template <typename T, int VEC> struct OutVec;
+template <typename T> struct OutVec<T, 1> {
+    static __device__ __forceinline__ void store(T *p, const float *v) { p[0] = from_float<T>(v[0]); }
+};
+template <typename T> struct OutVec<T, 2> {
+    static __device__ __forceinline__ void store(T *p, const float *v) {
+        p[0] = from_float<T>(v[0]);
+        p[1] = from_float<T>(v[1]);
+    }
+};
+template <> struct OutVec<float, 4> {
+    static __device__ __forceinline__ void store(float *p, const float *v) {
+        *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+};
+template <typename T> struct OutVec<T, 4> {
+    static __device__ __forceinline__ void store(T *p, const float *v) {
+        union { T h[4]; uint2 u; } x;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x.h[i] = from_float<T>(v[i]);
+        *reinterpret_cast<uint2 *>(p) = x.u;
+    }
+};
+
+template <int VEC> __device__ __forceinline__ void load_vec(const float *p, float *v) {
+    if constexpr (VEC == 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(p);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    } else if constexpr (VEC == 2) {
+        const float2 x = *reinterpret_cast<const float2 *>(p);
+        v[0] = x.x; v[1] = x.y;
+    } else {
+        v[0] = p[0];
+    }
+}
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256) merge_kernel(AttnArgs a, int use_list, int nrows) {
+    const int wid = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (wid >= nrows) return;
+    const int item = wid / a.hq, h = wid - item * a.hq;
     const int qi = use_list ? a.plan.decode[item] : item;
     const int S = a.splits;
-    __shared__ float w[PA_MAX_SPLITS];
-    __shared__ float wsum;
     const int64_t rows = (int64_t)a.plan.queries * a.hq;
     const int64_t row = (int64_t)qi * a.hq + h;
-    if (threadIdx.x < 32) {
-        // max and weights over the splits, one warp
-        float m = -INFINITY;
-        for (int s = threadIdx.x; s < S; s += 32) m = fmaxf(m, a.ws_lse[s * rows + row]);
-        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float tot = 0.f;
-        for (int s = threadIdx.x; s < S; s += 32) {
-            float l = a.ws_lse[s * rows + row];
-            float ws = (l == -INFINITY) ? 0.f : __expf(l - m);
-            w[s] = ws;
-            tot += ws;
-        }
-        for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-        if (threadIdx.x == 0) wsum = tot;
+    float m = -INFINITY;
+    for (int s = lane; s < S; s += 32) m = fmaxf(m, a.ws_lse[s * rows + row]);
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float tot = 0.f;
+    for (int s = lane; s < S; s += 32) {
+        const float l = a.ws_lse[s * rows + row];
+        tot += (l == -INFINITY) ? 0.f : __expf(l - m);
     }
-    __syncthreads();
-    const float inv = 1.f / wsum;
+    for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    const float inv = 1.f / tot;
     T *out = static_cast<T *>(a.out) + row * a.dv;
-    for (int c = threadIdx.x; c < a.dv; c += blockDim.x) {
-        float acc = 0.f;
+    for (int c = lane * VEC; c < a.dv; c += 32 * VEC) {
+        float acc[VEC];
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
+#pragma unroll 4
         for (int s = 0; s < S; ++s) {
-            float ws = w[s];
-            if (ws != 0.f) acc += ws * a.ws_o[(s * rows + row) * a.dv + c];
+            const float l = a.ws_lse[s * rows + row];
+            if (l == -INFINITY) continue;
+            const float ws = __expf(l - m);
+            float v[VEC];
+            load_vec<VEC>(a.ws_o + (s * rows + row) * a.dv + c, v);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) acc[i] += ws * v[i];
         }
-        out[c] = from_float<T>(acc * inv);
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) acc[i] *= inv;
+        OutVec<T, VEC>::store(out + c, acc);
+    }
+}
+
+template <int VEC> void launch_merge_vec(const AttnArgs &a, bool use_list, int nrows, cudaStream_t st) {
+    const unsigned blocks = (unsigned)((nrows + 7) / 8);
+    switch (a.dtype) {
+        case PA_F32: merge_kernel<float, VEC><<<blocks, 256, 0, st>>>(a, use_list, nrows); break;
+        case PA_F16: merge_kernel<__half, VEC><<<blocks, 256, 0, st>>>(a, use_list, nrows); break;
+        default: merge_kernel<__nv_bfloat16, VEC><<<blocks, 256, 0, st>>>(a, use_list, nrows); break;
     }
 }
 
 cudaError_t launch_merge(const AttnArgs &a, bool use_list, cudaStream_t st) {
     const int items = use_list ? a.plan.n_decode : a.plan.queries;
     if (items == 0) return cudaSuccess;
-    dim3 grid(items, a.hq);
-    switch (a.dtype) {
-        case PA_F32: merge_kernel<float><<<grid, 128, 0, st>>>(a, use_list); break;
-        case PA_F16: merge_kernel<__half><<<grid, 128, 0, st>>>(a, use_list); break;
-        default: merge_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(a, use_list); break;
-    }
+    const int nrows = items * a.hq;
+    // the workspace is 16-byte aligned and rows are dv floats apart; the output
+    // takes 4-wide stores only when its base allows them
+    const uintptr_t ob = reinterpret_cast<uintptr_t>(a.out);
+    const uintptr_t esz = a.dtype == PA_F32 ? 4 : 2;
+    if (a.dv % 4 == 0 && ob % (4 * esz) == 0)
+        launch_merge_vec<4>(a, use_list, nrows, st);
+    else if (a.dv % 2 == 0)
+        launch_merge_vec<2>(a, use_list, nrows, st);
+    else
+        launch_merge_vec<1>(a, use_list, nrows, st);
     return cudaGetLastError();
 }
 

@@ -119,6 +119,32 @@ def test_split_heuristic(built_lib):
     assert pka.paged_attn_split_heuristic(p, 64, 8, num_sms=152, window=4096) <= 4096 // 64
 
 
+def _mla_plan(lens):
+    """One decode query per history, pages laid out back to back (ps = 64)."""
+    pages = [(n + 63) // 64 for n in lens]
+    width = max(pages)
+    table, off = np.zeros((len(lens), width), dtype=np.int32), 0
+    for i, n in enumerate(pages):
+        table[i, :n] = np.arange(off, off + n)
+        off += n
+    return plan(lens, table, list(range(len(lens))), [n - 1 for n in lens], 64, off)
+
+
+def test_mla_split_heuristic(built_lib):
+    """The MLA kernel is tensor-bound: split only to fill SM pairs or to cut a dominant history."""
+    rng = np.random.default_rng(0)
+    many = _mla_plan([int(x) for x in rng.integers(1024, 16385, size=128)])
+    assert pka.paged_mla_split_heuristic(many, 128, num_sms=152) == 1        # 128 pairs already cover 76 slots
+    few = _mla_plan([8192] * 4)
+    s = pka.paged_mla_split_heuristic(few, 128, num_sms=152)
+    assert 19 <= s <= 8192 // 256                                            # 4 x s items fill 76 pair slots
+    skew = _mla_plan([131072] + [1024] * 100)                                # one history holds most keys
+    assert pka.paged_mla_split_heuristic(skew, 128, num_sms=152) > 1
+    assert pka.paged_mla_split_heuristic(few, 128, num_sms=152, window=1024) == 4   # >= 256 keys per split
+    assert pka.paged_mla_split_heuristic(_mla_plan([100]), 128, num_sms=152) == 1
+    assert 1 <= pka.paged_mla_split_heuristic(_mla_plan([1 << 20]), 128, num_sms=4096) <= 64
+
+
 def _lib():
     return pka.load()
 
