@@ -277,26 +277,47 @@ def soak_clocks(step: DecodeStep, device, seconds=1.0):
 
 
 def e2e_leg(case, device, steps: int, warmup: int):
-    """Same metric through the public API with host buffers: per step, upload the
-    plan and this step's inputs from pinned memory, append, attend, read the
-    result back (pinned) and wait for it."""
-    import paged_kv_attention_20_gb300 as pka
+    """Same metric through the public API with host buffers, as a serving loop
+    replays a decode step: per step the schedule's device image is staged into
+    pinned memory (Plan.stage), then one CUDA graph replay copies it and the
+    step's inputs (q, new_k, new_v) from pinned memory to the device, appends,
+    attends and copies the result back to pinned memory, and the host waits for
+    it.  Checked once against the same step run call by call."""
     step = DecodeStep(case, device)
     host = {k: getattr(case, k).pin_memory() for k in ("q", "new_k", "new_v")}
     out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    n = step.plan.device_bytes()
     words = step.plan.words
-    h2d = sum(t.numel() * t.element_size() for t in host.values()) + step.plan.device_bytes()
+    words_host = torch.empty(n, dtype=torch.uint8).pin_memory()
+    step.plan.stage(words_host, words)
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + n
     d2h = out_host.numel() * out_host.element_size()
 
-    def one():
-        step.plan.upload_into(words)
+    def body():
+        words[:n].copy_(words_host, non_blocking=True)
         step.dc.q.copy_(host["q"], non_blocking=True)
         step.dc.new_k.copy_(host["new_k"], non_blocking=True)
         step.dc.new_v.copy_(host["new_v"], non_blocking=True)
         step.store()
         step.attend()
         out_host.copy_(step.out, non_blocking=True)
-        torch.cuda.current_stream(device).synchronize()
+
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        body()                       # kernel attributes are set outside capture
+    torch.cuda.current_stream(device).wait_stream(side)
+    torch.cuda.synchronize(device)
+    eager = out_host.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+    stream = torch.cuda.current_stream(device)
+
+    def one():
+        step.plan.stage(words_host, words)
+        graph.replay()
+        stream.synchronize()
 
     for _ in range(warmup):
         one()
@@ -304,9 +325,13 @@ def e2e_leg(case, device, steps: int, warmup: int):
     for _ in range(steps):
         one()
     dt = time.perf_counter() - t
-    del pka
+    if not torch.equal(out_host, eager) or step.pka.device_status() != 0:
+        raise RuntimeError("graph-replayed step differs from the call-by-call step")
     return {"value": kv_bytes(case) * steps / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": dt / steps * 1e3}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": dt / steps * 1e3,
+            "mode": "per step: Plan.stage into pinned memory, one CUDA graph replay (pinned H2D of the plan "
+                    "image, q, new_k, new_v; paged_kv_store; paged_attn_forward_split; D2H of the output), "
+                    "host wait"}
 
 
 def secondary(device, warmup: int, steps: int, peaks, which):

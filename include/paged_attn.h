@@ -59,7 +59,7 @@ typedef enum {
 
 typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
 
-#define PA_ABI_VERSION 2
+#define PA_ABI_VERSION 3
 #define PA_MAX_SPLITS 64                        /* `MAX_SPLITS` of the split workspace      */
 #define PA_MAX_HEAD_DIM 1024                    /* d, dv <= 1024 (`execute_attention_into`) */
 #define PA_MAX_POS_DIM 256                      /* MLA position dim P <= 256                */
@@ -121,6 +121,25 @@ size_t pa_plan_device_bytes(const pa_plan *plan);
  * after it.
  */
 pa_status pa_plan_upload(pa_plan *plan, void *device_words, size_t bytes, pa_stream_t stream);
+
+/*
+ * Stage a plan for a copy the caller makes: write its device image
+ * (pa_plan_device_bytes bytes, the same bytes pa_plan_upload copies) into the
+ * caller's host buffer `host_words` (typically pinned memory) and bind
+ * `device_words` as the plan's device copy, without touching the device.  The
+ * caller then moves host_words to device_words with its own stream-ordered
+ * copy before the next call that uses the plan; a copy from pinned memory can
+ * be captured in a CUDA graph, so one replay can refresh the schedule, append
+ * and attend (the `DevicePlan` schedule re-sent each step with no host
+ * synchronisation on the way).  Both buffers are caller-owned and at least
+ * pa_plan_device_bytes long; device_words is 16-byte aligned and stays alive
+ * while the plan is used.  PA_ERR_ARG on a null pointer, a short buffer or a
+ * misaligned device buffer (nothing is written then).  A graph captured around
+ * calls on this plan stays valid for images of plans with the same counts
+ * (pa_plan_describe) and the same device buffer.
+ */
+pa_status pa_plan_stage(pa_plan *plan, void *host_words, size_t host_bytes, void *device_words,
+                        size_t device_bytes);
 
 /* Free the host side of a plan (does not touch the caller's device buffer). */
 void pa_plan_destroy(pa_plan *plan);

@@ -28,7 +28,7 @@ _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 MAX_SPLITS = 64
 
 EXPORTED = ["pa_last_error", "pa_status_string", "pa_abi_version", "paged_attn_plan",
-            "pa_plan_device_bytes", "pa_plan_upload", "pa_plan_destroy", "pa_plan_describe",
+            "pa_plan_device_bytes", "pa_plan_upload", "pa_plan_stage", "pa_plan_destroy", "pa_plan_describe",
             "pa_workspace_bytes", "paged_attn_split_heuristic", "paged_mla_split_heuristic", "paged_kv_store", "paged_attn_forward",
             "paged_attn_forward_split", "paged_mla_forward", "pa_plan_advance", "pa_time_next_kernel",
             "pa_device_status"]
@@ -67,6 +67,8 @@ def load() -> ctypes.CDLL:
     lib.pa_plan_device_bytes.restype = sz
     lib.pa_plan_upload.argtypes = [vp, vp, sz, vp]
     lib.pa_plan_upload.restype = ctypes.c_int
+    lib.pa_plan_stage.argtypes = [vp, vp, sz, vp, sz]
+    lib.pa_plan_stage.restype = ctypes.c_int
     lib.pa_plan_destroy.argtypes = [vp]
     lib.pa_plan_destroy.restype = None
     lib.pa_plan_describe.argtypes = [vp, ctypes.POINTER(i64)]
@@ -145,6 +147,22 @@ class Plan:
         self.words = words
         self.device = words.device
         _check(load().pa_plan_upload(self._handle, words.data_ptr(), words.numel(), _stream(words.device)))
+        return self
+
+    def stage(self, host_words: torch.Tensor, device_words: torch.Tensor) -> "Plan":
+        """Write the device image into `host_words` (CPU uint8, e.g. pinned) and bind `device_words`.
+
+        Nothing is copied to the device: the caller copies host_words into
+        device_words on its stream (capturable in a CUDA graph) before the
+        next call that uses this plan.
+        """
+        for t, name, on_cuda in ((host_words, "host_words", False), (device_words, "device_words", True)):
+            if t.dtype != torch.uint8 or not t.is_contiguous() or t.is_cuda != on_cuda:
+                raise ValueError(f"{name} must be a contiguous uint8 {'CUDA' if on_cuda else 'CPU'} tensor")
+        _check(load().pa_plan_stage(self._handle, host_words.data_ptr(), host_words.numel(),
+                                    device_words.data_ptr(), device_words.numel()))
+        self.words = device_words
+        self.device = device_words.device
         return self
 
     def __del__(self):

@@ -255,6 +255,17 @@ pa_status pa_plan_upload(pa_plan *plan, void *device_words, size_t bytes, pa_str
     return PA_OK;
 }
 
+pa_status pa_plan_stage(pa_plan *plan, void *host_words, size_t host_bytes, void *device_words,
+                        size_t device_bytes) {
+    if (!plan || !host_words || !device_words) return fail(PA_ERR_ARG, "pa_plan_stage: null argument");
+    if (!aligned16(device_words)) return fail(PA_ERR_ARG, "pa_plan_stage: device buffer not 16-byte aligned");
+    const size_t need = pa_plan_device_bytes(plan);
+    if (host_bytes < need || device_bytes < need) return fail(PA_ERR_ARG, "pa_plan_stage: buffer too small");
+    std::memcpy(host_words, plan->words.data(), need);
+    plan->dev = static_cast<const int32_t *>(device_words);
+    return PA_OK;
+}
+
 void pa_plan_destroy(pa_plan *plan) { delete plan; }
 
 pa_status pa_plan_describe(const pa_plan *plan, int64_t out[8]) {

@@ -33,7 +33,7 @@ def test_header_functions_are_exported(built_lib):
     for n in names:
         assert hasattr(built_lib, n), f"{n} declared in paged_attn.h but not exported"
     assert set(pka.EXPORTED) <= set(names)
-    assert built_lib.pa_abi_version() == 2
+    assert built_lib.pa_abi_version() == 3
 
 
 def _status_of(fn, *a, **k):
@@ -117,6 +117,30 @@ def test_split_heuristic(built_lib):
     # a sliding window bounds the history the heuristic splits
     assert pka.paged_attn_split_heuristic(p, 64, 8, num_sms=152, window=64) == 1
     assert pka.paged_attn_split_heuristic(p, 64, 8, num_sms=152, window=4096) <= 4096 // 64
+
+
+def test_plan_stage_writes_the_device_image(built_lib):
+    """pa_plan_stage: the image goes to a host buffer, the device buffer is only bound."""
+    import torch
+    lens, table = [5, 40], [[3, -1, -1], [2, 4, 1]]
+    p = plan(lens, np.array(table), [0, 1, 1], [4, 38, 39], 16, 5)
+    n = p.device_bytes()
+    host = torch.zeros(n + 64, dtype=torch.uint8)
+    fake = 0x10000                                     # bound, never dereferenced on the host
+    lib = _lib()
+    assert lib.pa_plan_stage(p.handle, host.data_ptr(), n + 64, ctypes.c_void_p(fake), n) == 0
+    words = host[:n].view(torch.int32).numpy()
+    assert np.all(host[n:].numpy() == 0)               # nothing past the image is written
+    flat = np.array(table, dtype=np.int32).ravel()
+    hits = [i for i in range(words.size - flat.size + 1) if np.array_equal(words[i:i + flat.size], flat)]
+    assert hits and hits[0] % 4 == 0                   # the block table sits in a 16-byte aligned section
+    again = torch.zeros(n, dtype=torch.uint8)
+    assert lib.pa_plan_stage(p.handle, again.data_ptr(), n, ctypes.c_void_p(fake), n) == 0
+    assert torch.equal(again, host[:n])
+    assert lib.pa_plan_stage(p.handle, host.data_ptr(), n - 1, ctypes.c_void_p(fake), n) == 1   # short host
+    assert lib.pa_plan_stage(p.handle, host.data_ptr(), n, ctypes.c_void_p(fake), n - 16) == 1  # short device
+    assert lib.pa_plan_stage(p.handle, host.data_ptr(), n, ctypes.c_void_p(fake + 4), n) == 1   # misaligned
+    assert lib.pa_plan_stage(p.handle, None, n, ctypes.c_void_p(fake), n) == 1
 
 
 def _mla_plan(lens):

@@ -17,8 +17,8 @@ import torch
 
 import oracle
 import paged_kv_attention_20_gb300 as pka
-from helpers import assert_close
-from workloads import build_case
+from helpers import assert_close, oracle_after_store
+from workloads import build_case, decode_queries
 
 pytestmark = pytest.mark.gpu
 
@@ -83,3 +83,50 @@ def test_advance_past_reserved_pages_is_flagged(cuda_device):
     pka.paged_attn_plan_advance(plan)
     torch.cuda.synchronize()
     assert pka.device_status(clear=True) == 4
+
+
+def test_staged_plans_replayed_from_one_graph(cuda_device):
+    """Plan.stage + a pinned copy inside the graph: each replay runs the schedule staged last.
+
+    Two plans with the same counts but different page assignments (and caches)
+    are staged in turn into the same pinned and device buffers; every replay is
+    checked against the oracle for the plan staged before it.
+    """
+    seq_lens = [70, 333, 5, 1000]
+    queries = decode_queries(seq_lens) + [(3, 500)]
+    cases = [build_case("staged", seed, seq_lens, queries, 16, 4, 128, 128, 16, torch.bfloat16,
+                        1 / math.sqrt(128)) for seed in (71, 72)]
+    plans = [pka.paged_attn_plan(c.seq_lens, c.block_table, c.query_seq, c.query_pos, c.page_size, c.num_pages,
+                                 upload=False) for c in cases]
+    assert plans[0].device_bytes() == plans[1].device_bytes()
+    n = plans[0].device_bytes()
+    dev = torch.device("cuda")
+    words = torch.empty(n, dtype=torch.uint8, device=dev)
+    words_host = torch.empty(n, dtype=torch.uint8).pin_memory()
+    dc = cases[0].to(dev)
+    out = torch.empty(cases[0].num_queries, 16, 128, dtype=torch.bfloat16, device=dev)
+    plans[0].stage(words_host, words)
+    ws = pka.make_workspace(plans[0], 16, 128, 3)
+    state = {"plan": plans[0]}
+
+    def body():
+        words.copy_(words_host, non_blocking=True)
+        pka.paged_kv_store(state["plan"], dc.new_k, dc.new_v, dc.k_cache, dc.v_cache)
+        pka.paged_attn_forward_split(state["plan"], dc.q, dc.k_cache, dc.v_cache, cases[0].scale, 3,
+                                     workspace=ws, out=out)
+
+    body()                             # one plain run first (kernel attributes are set outside capture)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+    for i in (1, 0, 1):
+        c = cases[i]
+        plans[i].stage(words_host, words)          # host-side only; the replay copies it
+        for name in ("q", "k_cache", "v_cache", "new_k", "new_v"):
+            getattr(dc, name).copy_(getattr(c, name))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pka.device_status() == 0
+        ref, _, _, _ = oracle_after_store(c)
+        assert_close(out.cpu().double().numpy(), ref, torch.bfloat16, f"staged plan {i}")
