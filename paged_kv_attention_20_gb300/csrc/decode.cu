@@ -512,6 +512,7 @@ cudaError_t launch_generic(const AttnArgs &a, int items, int use_list, cudaStrea
 cudaError_t launch_decode(const AttnArgs &a, bool use_decode_list, cudaStream_t st) {
     const int items = use_decode_list ? a.plan.n_decode : a.plan.queries;
     if (items == 0) return cudaSuccess;
+    if (decode_tc_supported(a)) return launch_decode_tc(a, use_decode_list, st);
     if (decode_tma_supported(a)) return launch_decode_tma(a, use_decode_list, st);
     const bool fast = a.dtype != PA_F32 && a.p == 0 && a.d == a.dv &&
                       (a.d == 64 || a.d == 128 || a.d == 256) && aligned16(a.q) && aligned16(a.k) &&

@@ -97,6 +97,8 @@ cudaError_t launch_decode(const AttnArgs &a, bool use_decode_list, cudaStream_t 
 // Warp-independent TMA decode (bf16/f16, D == Dv in {64,128,256}, power-of-two pages).
 bool decode_tma_supported(const AttnArgs &a);
 cudaError_t launch_decode_tma(const AttnArgs &a, bool use_decode_list, cudaStream_t st);
+bool decode_tc_supported(const AttnArgs &a);
+cudaError_t launch_decode_tc(const AttnArgs &a, bool use_decode_list, cudaStream_t st);
 cudaError_t launch_merge(const AttnArgs &a, bool use_decode_list, cudaStream_t st);
 // Tensor-core prefill over plan.tiles; returns cudaErrorNotSupported when the
 // shape/dtype is outside what the kernel covers (caller then uses decode for all).
