@@ -6,7 +6,12 @@
 // consecutive positions of one sequence; query i of a chunk at position p_i
 // sees keys 0..p_i: the cached context plus the chunk's earlier rows.
 //
-// One CTA per (tile of up to 128 consecutive queries, query head):
+// Work unit: (tile of up to 128 consecutive queries, split, query head).  The
+// kernel is persistent: as many clusters as fit on the GPU at once, each
+// walking every n-th unit (heaviest first), so the K/V rings stream on from
+// one unit into the next, Q of the next unit loads while the last tiles of
+// the current one finish, and a CTA's start-up and teardown are paid once
+// (as one CTA per unit, they cost ~4 µs of every 17-tile unit).  Per unit:
 //   warps 0-7  softmax / O correction / epilogue: query row r (TMEM lane r) is
 //              shared by warps r/32 and r/32+4, each taking 64 of the 128 key
 //              (and output) columns; row maxima and sums cross over shared memory;
@@ -59,7 +64,9 @@ struct Smem {
     uint8_t q[kTileBytes];
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kTileBytes];
-    uint64_t q_full;
+    uint64_t q_full;               // Q of the CTA's current unit landed (phase = unit parity)
+    uint64_t q_empty;              // every S MMA of the unit done: the Q buffer may be refilled
+    uint64_t o_free;               // the softmax warps have read O of the unit (all 256 threads)
     uint64_t k_full[kStages];      // K tile landed
     uint64_t k_empty[kStages];     // S of the tile done in every CTA of the cluster (K free)
     uint64_t v_full[kStages];
@@ -123,40 +130,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     Smem &s = *reinterpret_cast<Smem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // Heaviest tiles first: the plan orders tiles by decreasing key count.
-    // block = (tile * splits + split) * Hq + head
-    const int tile_idx = blockIdx.x / (prm.hq * prm.splits);
-    const int split = (blockIdx.x / prm.hq) % prm.splits;
-    const int h = blockIdx.x % prm.hq;
-    const int kvh = h / (prm.hq / prm.hkv);
-    const int4 tile = prm.plan.tiles[tile_idx];
-    const int seq = tile.x, q0 = tile.y, nq = tile.z, pos0 = tile.w;
-    const int ps = prm.plan.page_size;
-    const int seq_len = prm.plan.seq_lens[seq];
-    const int last_pos = pos0 + nq - 1;
-    // Keys of row r for this split: its visible range [lo, hi) (causal end,
-    // sliding window) cut by the split partition.  Both ends grow with the
-    // row's position, so the tile's key range runs from the first row's lower
-    // end to the last row's upper end: key tiles kt0 .. kt0 + n_kt - 1.
-    auto row_keys = [&](int pos, int64_t &j0, int64_t &j1) {
-        int64_t lo, hi;
-        visible_range(pos, seq_len, prm.causal, prm.window, lo, hi);
-        split_bounds(lo, hi, prm.splits, split, ps, j0, j1);
-    };
-    int64_t first_j0, first_j1, last_j0, last_j1;
-    row_keys(pos0, first_j0, first_j1);
-    row_keys(last_pos, last_j0, last_j1);
-    const int kt0 = (int)(first_j0 / kN);
-    const int n_kt = last_j1 > first_j0 ? (int)((last_j1 + kN - 1) / kN) - kt0 : 0;
-    const int32_t *trow = prm.plan.table + (int64_t)seq * prm.plan.width;
-    // CTAs of one cluster hold query heads of the same KV head and the same
-    // query tile: they walk the same key tiles, and each K/V tile is loaded once
-    // for all of them (multicast), every CTA issuing a share of its boxes.
+    // Persistent: cluster c of C walks units c, c + C, c + 2C, ... of U, a unit
+    // being (query tile, split, csize consecutive query heads) in the order
+    // block = (tile * splits + split) * Hq + head; the plan orders tiles by
+    // decreasing key count, so the heaviest units go first.  Every role walks
+    // the same units; ring stages, S buffers and their barrier phases follow
+    // one tile counter that runs on across units, so the K/V rings stream
+    // without a break from one unit into the next.
     const uint32_t crank = cluster_ctarank(), csize = cluster_nctarank();
     const uint16_t cmask = (uint16_t)((1u << csize) - 1u);
+    const int cluster = (int)(blockIdx.x / csize);
+    const int n_clusters = (int)(gridDim.x / csize);
+    const int units = prm.plan.n_tiles * prm.splits * prm.hq / (int)csize;
+    const int ps = prm.plan.page_size;
+    struct Unit {
+        int split, h, kvh, q0, nq, pos0, seq_len, kt0, n_kt;
+        const int32_t *trow;
+    };
+    // Keys of a row of the unit's split: its visible range [lo, hi) (causal
+    // end, sliding window) cut by the split partition.  Both ends grow with
+    // the row's position, so the tile's key range runs from the first row's
+    // lower end to the last row's upper end: key tiles kt0 .. kt0 + n_kt - 1.
+    auto row_keys = [&](const Unit &u, int pos, int64_t &j0, int64_t &j1) {
+        int64_t lo, hi;
+        visible_range(pos, u.seq_len, prm.causal, prm.window, lo, hi);
+        split_bounds(lo, hi, prm.splits, u.split, ps, j0, j1);
+    };
+    auto unit_at = [&](int ui) -> Unit {
+        Unit u;
+        const int b = ui * (int)csize + (int)crank;
+        const int tile_idx = b / (prm.hq * prm.splits);
+        u.split = (b / prm.hq) % prm.splits;
+        u.h = b % prm.hq;
+        u.kvh = u.h / (prm.hq / prm.hkv);
+        const int4 tile = prm.plan.tiles[tile_idx];
+        const int seq = tile.x;
+        u.q0 = tile.y;
+        u.nq = tile.z;
+        u.pos0 = tile.w;
+        u.seq_len = prm.plan.seq_lens[seq];
+        u.trow = prm.plan.table + (int64_t)seq * prm.plan.width;
+        int64_t first_j0, first_j1, last_j0, last_j1;
+        row_keys(u, u.pos0, first_j0, first_j1);
+        row_keys(u, u.pos0 + u.nq - 1, last_j0, last_j1);
+        u.kt0 = (int)(first_j0 / kN);
+        u.n_kt = last_j1 > first_j0 ? (int)((last_j1 + kN - 1) / kN) - u.kt0 : 0;
+        return u;
+    };
 
     if (tid == 0) {
         mbar_init(&s.q_full, 1);
+        mbar_init(&s.q_empty, 1);
+        mbar_init(&s.o_free, 2 * kM);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&s.k_full[i], 1);
             mbar_init(&s.k_empty[i], csize);       // one release per CTA of the cluster
@@ -186,12 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 8 || warp == 10) {
         // ------------------------------------------------- TMA producers --
-        // Warp 8 streams K (and Q once), warp 10 streams V, each through its own
-        // 3-stage ring: a K stage is free as soon as S of its tile is computed,
-        // a V stage only after P.V, so K runs ahead of V.  Lane 0 owns the
-        // barriers; lanes 0..pages_per_tile-1 each gather one page (two
+        // Warp 8 streams K (and Q of each unit), warp 10 streams V, each through
+        // its own 3-stage ring: a K stage is free as soon as S of its tile is
+        // computed, a V stage only after P.V, so K runs ahead of V.  Lane 0 owns
+        // the barriers; lanes 0..pages_per_tile-1 each gather one page (two
         // 64-column boxes).  In a cluster, box j of page p is issued by CTA
-        // (2p + j) % csize and multicast to all.
+        // (2p + j) % csize and multicast to all.  Q of the next unit is loaded
+        // once every S MMA of the previous unit has completed.
         const bool is_k = warp == 8;
         const int pages_per_tile = kN / ps;
         const CUtensorMap *tm = is_k ? &tm_k : &tm_v;
@@ -199,48 +225,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t *empty = is_k ? s.k_empty : s.v_empty;
         if (lane == 0) {
             tma_prefetch_desc(tm);
-            if (is_k) {
-                tma_prefetch_desc(&tm_q);
-                mbar_arrive_expect_tx(&s.q_full, kTileBytes);
-                tma_load_3d(s.q, &tm_q, 0, h, q0, &s.q_full);
-                tma_load_3d(s.q + kHalfBytes, &tm_q, 64, h, q0, &s.q_full);
-            }
+            if (is_k) tma_prefetch_desc(&tm_q);
         }
         const int oob_row = prm.plan.pages * ps;          // rows >= this read as zeros
-        const int used_pages = (seq_len + ps - 1) / ps;
-        for (int kt = 0; kt < n_kt; ++kt) {
-            const int st = kt % kStages;
-            uint8_t *ring = is_k ? s.k[st] : s.v[st];
-            bool go = true;
-            if (lane == 0) {
-                if (kt >= kStages && !mbar_wait(&empty[st], ((kt / kStages) - 1) & 1)) {
+        int gt = 0;                                        // tiles streamed so far (all units)
+        bool go = true;
+        for (int ui = cluster, i = 0; go && ui < units; ui += n_clusters, ++i) {
+            const Unit u = unit_at(ui);
+            if (is_k && lane == 0) {
+                if (i > 0 && !mbar_wait(&s.q_empty, (i - 1) & 1)) {
                     set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
                     go = false;
                 } else {
-                    mbar_arrive_expect_tx(&full[st], kTileBytes);
+                    mbar_arrive_expect_tx(&s.q_full, kTileBytes);
+                    tma_load_3d(s.q, &tm_q, 0, u.h, u.q0, &s.q_full);
+                    tma_load_3d(s.q + kHalfBytes, &tm_q, 64, u.h, u.q0, &s.q_full);
                 }
             }
             go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
-            if (!go) break;
-            if (lane < pages_per_tile) {
-                const int lp = (kt0 + kt) * pages_per_tile + lane;
-                const int row = lp < used_pages ? trow[lp] * ps : oob_row;
-                const uint32_t off = (uint32_t)lane * ps * 128;
+            const int used_pages = (u.seq_len + ps - 1) / ps;
+            for (int kt = 0; go && kt < u.n_kt; ++kt, ++gt) {
+                const int st = gt % kStages;
+                uint8_t *ring = is_k ? s.k[st] : s.v[st];
+                if (lane == 0) {
+                    if (gt >= kStages && !mbar_wait(&empty[st], ((gt / kStages) - 1) & 1)) {
+                        set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
+                        go = false;
+                    } else {
+                        mbar_arrive_expect_tx(&full[st], kTileBytes);
+                    }
+                }
+                go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+                if (!go) break;
+                if (lane < pages_per_tile) {
+                    const int lp = (u.kt0 + kt) * pages_per_tile + lane;
+                    const int row = lp < used_pages ? u.trow[lp] * ps : oob_row;
+                    const uint32_t off = (uint32_t)lane * ps * 128;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    if (csize == 1) {
-                        tma_load_3d(ring + j * kHalfBytes + off, tm, j * 64, kvh, row, &full[st]);
-                    } else if ((uint32_t)((2 * lane + j) % (int)csize) == crank) {
-                        tma_load_3d_multicast(ring + j * kHalfBytes + off, tm, j * 64, kvh, row, &full[st], cmask);
+                    for (int j = 0; j < 2; ++j) {
+                        if (csize == 1) {
+                            tma_load_3d(ring + j * kHalfBytes + off, tm, j * 64, u.kvh, row, &full[st]);
+                        } else if ((uint32_t)((2 * lane + j) % (int)csize) == crank) {
+                            tma_load_3d_multicast(ring + j * kHalfBytes + off, tm, j * 64, u.kvh, row, &full[st],
+                                                  cmask);
+                        }
                     }
                 }
             }
         }
         // With a cluster, peers release stages by remote arrivals: wait for the
         // last ones so none lands after this CTA has exited.
-        if (csize > 1 && lane == 0) {
-            for (int kt = max(0, n_kt - kStages); kt < n_kt; ++kt)
-                if (!mbar_wait(&empty[kt % kStages], (kt / kStages) & 1)) {
+        if (go && csize > 1 && lane == 0) {
+            for (int t = max(0, gt - kStages); t < gt; ++t)
+                if (!mbar_wait(&empty[t % kStages], (t / kStages) & 1)) {
                     set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
                     break;
                 }
@@ -248,53 +285,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 9 || warp == 11) {
         // ------------------------------------------------------ MMA issuers --
         // Two issuing threads: warp 9 issues S = Q K^T (three TMEM buffers, so
-        // S runs up to two tiles ahead of P.V), warp 11 issues O += P V as soon
-        // as P of a tile is in TMEM.  The tensor core accepts only a few MMAs
-        // ahead, so a single issuer spends most of a tile blocked on one kind
-        // and notices the other late.  The two touch different TMEM (S buffers
-        // vs O) and shared memory (K vs V), and each commits its own MMAs.
+        // S runs up to two tiles ahead of P.V, into the next unit as well), warp
+        // 11 issues O += P V as soon as P of a tile is in TMEM.  The tensor core
+        // accepts only a few MMAs ahead, so a single issuer spends most of a tile
+        // blocked on one kind and notices the other late.  The two touch
+        // different TMEM (S buffers vs O) and shared memory (K vs V), and each
+        // commits its own MMAs.  P.V of a unit's first tile overwrites O, so it
+        // waits until the softmax warps have read O of the previous unit.
         if (lane == 0) {
             bool ok = true;
+            int gt = 0;
             if (warp == 9) {
                 const uint32_t idesc_s = idesc_f16(kM, kN, prm.bf16 != 0, false, false);
                 const uint32_t q_addr = smem_u32(s.q);
-                ok = mbar_wait(&s.q_full, 0);
-                for (int kt = 0; ok && kt < n_kt; ++kt) {
-                    const int st = kt % kStages, sb = kt % 3;
-                    if (!mbar_wait(&s.k_full[st], (kt / kStages) & 1)) { ok = false; break; }
-                    // the buffer's previous tile (kt-3) must be through its P.V (P lives in it)
-                    if (kt >= 3 && !mbar_wait(&s.o_done[sb], ((kt / 3) - 1) & 1)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t k_addr = smem_u32(s.k[st]);
-                    for (int ks = 0; ks < kD / 16; ++ks) {
-                        const uint32_t o = (ks / 4) * kHalfBytes + (ks % 4) * 32;
-                        mma_f16_ss(tmem_s(sb), smem_desc(q_addr + o, 16, 1024, kLayoutSwizzle128B),
-                                   smem_desc(k_addr + o, 16, 1024, kLayoutSwizzle128B), idesc_s, ks > 0 ? 1u : 0u);
+                for (int ui = cluster, i = 0; ok && ui < units; ui += n_clusters, ++i) {
+                    const Unit u = unit_at(ui);
+                    if (!mbar_wait(&s.q_full, i & 1)) { ok = false; break; }
+                    for (int kt = 0; kt < u.n_kt; ++kt, ++gt) {
+                        const int st = gt % kStages, sb = gt % 3;
+                        if (!mbar_wait(&s.k_full[st], (gt / kStages) & 1)) { ok = false; break; }
+                        // the buffer's previous tile (gt-3) must be through its P.V (P lives in it)
+                        if (gt >= 3 && !mbar_wait(&s.o_done[sb], ((gt / 3) - 1) & 1)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t k_addr = smem_u32(s.k[st]);
+                        for (int ks = 0; ks < kD / 16; ++ks) {
+                            const uint32_t o = (ks / 4) * kHalfBytes + (ks % 4) * 32;
+                            mma_f16_ss(tmem_s(sb), smem_desc(q_addr + o, 16, 1024, kLayoutSwizzle128B),
+                                       smem_desc(k_addr + o, 16, 1024, kLayoutSwizzle128B), idesc_s,
+                                       ks > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&s.s_full[sb]);
+                        if (csize == 1)
+                            mma_commit(&s.k_empty[st]);
+                        else
+                            mma_commit_multicast(&s.k_empty[st], cmask);   // this CTA's copy of the K stage is free
                     }
-                    mma_commit(&s.s_full[sb]);
-                    if (csize == 1)
-                        mma_commit(&s.k_empty[st]);
-                    else
-                        mma_commit_multicast(&s.k_empty[st], cmask);   // this CTA's copy of the K stage is free
+                    if (!ok) break;
+                    mma_commit(&s.q_empty);        // Q is free once this unit's S MMAs are done
                 }
             } else {
                 const uint32_t idesc_o = idesc_f16(kM, kD, prm.bf16 != 0, false, true);
-                for (int kt = 0; ok && kt < n_kt; ++kt) {
-                    const int st = kt % kStages;
-                    if (!mbar_wait(&s.p_ready[kt % 3], (kt / 3) & 1)) { ok = false; break; }
-                    if (!mbar_wait(&s.v_full[st], (kt / kStages) & 1)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t v_addr = smem_u32(s.v[st]);
-                    const uint32_t p_tmem = tmem_s(kt % 3);          // P (16-bit pairs) over the S columns
-                    for (int ks = 0; ks < kN / 16; ++ks) {
-                        const uint64_t b = smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, kLayoutSwizzle128B);
-                        mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
+                for (int ui = cluster, i = 0; ok && ui < units; ui += n_clusters, ++i) {
+                    const Unit u = unit_at(ui);
+                    if (i > 0 && !mbar_wait(&s.o_free, (i - 1) & 1)) { ok = false; break; }
+                    for (int kt = 0; kt < u.n_kt; ++kt, ++gt) {
+                        const int st = gt % kStages;
+                        if (!mbar_wait(&s.p_ready[gt % 3], (gt / 3) & 1)) { ok = false; break; }
+                        if (!mbar_wait(&s.v_full[st], (gt / kStages) & 1)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t v_addr = smem_u32(s.v[st]);
+                        const uint32_t p_tmem = tmem_s(gt % 3);          // P (16-bit pairs) over the S columns
+                        for (int ks = 0; ks < kN / 16; ++ks) {
+                            const uint64_t b = smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, kLayoutSwizzle128B);
+                            mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&s.o_done[gt % 3]);
+                        if (csize == 1)
+                            mma_commit(&s.v_empty[st]);
+                        else
+                            mma_commit_multicast(&s.v_empty[st], cmask);   // this CTA's copy of the V stage is free
                     }
-                    mma_commit(&s.o_done[kt % 3]);
-                    if (csize == 1)
-                        mma_commit(&s.v_empty[st]);
-                    else
-                        mma_commit_multicast(&s.v_empty[st], cmask);   // this CTA's copy of the V stage is free
                 }
             }
             if (!ok) set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_MMA);
@@ -307,13 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = 32 * q4 + lane;            // query row == TMEM lane
         const int col0 = 64 * h2;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-        const int my_pos = pos0 + r;
-        int64_t row_j0 = 0, row_j1 = 0;           // this row's keys in this split: [vis_lo, vis_end)
-        if (r < nq) row_keys(my_pos, row_j0, row_j1);   // rows past the tile's queries see nothing
-        const int vis_lo = (int)row_j0, vis_end = (int)row_j1;
-        float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         int xphase = 0;
+        int gt = 0;                                // tiles consumed so far (all units)
         // value of the other warp of this row (bounded waits; false on timeout)
         // One barrier round per exchange: slot n % 2 is written again at exchange
         // n + 2 only after the partner arrived for exchange n + 1, which it does
@@ -327,152 +373,162 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++xphase;
             return true;
         };
-        for (int kt = 0; kt < n_kt && ok; ++kt) {
-            const int sb = kt % 3;
-            ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[sb], (kt / 3) & 1));
-            if (!ok) break;
-            tc_fence_after();
-            const int kbase = (kt0 + kt) * kN + col0;
-            // my 64 scores of the row into registers (two loads, one wait)
-            uint32_t sv[64];
-            tmem_ld32(tmem_s(sb) + lane_off + col0, sv);
-            tmem_ld32(tmem_s(sb) + lane_off + col0 + 32, sv + 32);
-            tmem_wait_ld();
-            // keys outside the row's visible range score -inf (diagonal, sequence-end
-            // and window-edge tiles only)
-            if (kbase + 64 > vis_end || kbase < vis_lo) {
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (kbase + c >= vis_end || kbase + c < vis_lo) sv[c] = 0xff800000u;
-            }
-            // row maximum of the raw scores (the scale is positive, so it commutes with max)
-            float ma = -INFINITY, mb = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-                ma = fmax3(ma, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-                mb = fmax3(mb, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
-            }
-            const float mine = fmaxf(ma, mb) * prm.scale_log2;
-            float other;
-            ok = exchange(mine, other);
-            if (!ok) break;
-            const float mt = fmaxf(mine, other);
-            float alpha = 1.f;
-            if (mt > m_ref + kSlack) {
-                alpha = exp2f(m_ref - mt);
-                m_ref = mt;
-            }
-            // rescaling O needs the previous P.V finished (rare: the row max moved by > 2^8)
-            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(kt - 1) % 3], ((kt - 1) / 3) & 1));
+        for (int ui = cluster; ok && ui < units; ui += n_clusters) {
+            const Unit u = unit_at(ui);
+            int64_t row_j0 = 0, row_j1 = 0;           // this row's keys in this split: [vis_lo, vis_end)
+            if (r < u.nq) row_keys(u, u.pos0 + r, row_j0, row_j1);   // rows past the tile's queries see nothing
+            const int vis_lo = (int)row_j0, vis_end = (int)row_j1;
+            float m_ref = -INFINITY, l = 0.f;
+            for (int kt = 0; kt < u.n_kt && ok; ++kt, ++gt) {
+                const int sb = gt % 3;
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[sb], (gt / 3) & 1));
                 if (!ok) break;
                 tc_fence_after();
+                const int kbase = (u.kt0 + kt) * kN + col0;
+                // my 64 scores of the row into registers (two loads, one wait)
+                uint32_t sv[64];
+                tmem_ld32(tmem_s(sb) + lane_off + col0, sv);
+                tmem_ld32(tmem_s(sb) + lane_off + col0 + 32, sv + 32);
+                tmem_wait_ld();
+                // keys outside the row's visible range score -inf (diagonal, sequence-end
+                // and window-edge tiles only)
+                if (kbase + 64 > vis_end || kbase < vis_lo) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (kbase + c >= vis_end || kbase + c < vis_lo) sv[c] = 0xff800000u;
+                }
+                // row maximum of the raw scores (the scale is positive, so it commutes with max)
+                float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 64; c += 4) {
+                    ma = fmax3(ma, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+                    mb = fmax3(mb, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+                }
+                const float mine = fmaxf(ma, mb) * prm.scale_log2;
+                float other;
+                ok = exchange(mine, other);
+                if (!ok) break;
+                const float mt = fmaxf(mine, other);
+                float alpha = 1.f;
+                if (mt > m_ref + kSlack) {
+                    alpha = exp2f(m_ref - mt);
+                    m_ref = mt;
+                }
+                // rescaling O needs the previous P.V finished (rare: the row max moved by > 2^8)
+                if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(gt - 1) % 3], ((gt - 1) / 3) & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 64; c += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem_o + lane_off + col0 + c, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        tmem_st16(tmem_o + lane_off + col0 + c, v);
+                    }
+                    tmem_wait_st();
+                }
+                // P = exp2(s * scale - m_ref) as 16-bit pairs over my S columns (already in
+                // registers); masked keys hold -inf and give 0.  A row whose window has
+                // not started yet still has m_ref = -inf: its weights are all 0.
+                const float2 sc2 = make_float2(prm.scale_log2, prm.scale_log2);
+                const float mr = m_ref == -INFINITY ? 0.f : m_ref;
+                const float2 nm2 = make_float2(-mr, -mr);
+                float2 ls2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < 64; c += 32) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 x = ffma2(make_float2(__uint_as_float(sv[c + 2 * i]), __uint_as_float(sv[c + 2 * i + 1])),
+                                               sc2, nm2);
+                        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                        ls2 = fadd2(ls2, pp);
+                        pk[i] = pack2<T>(pp.x, pp.y);
+                    }
+                    tmem_st16(tmem_s(sb) + lane_off + (col0 + c) / 2, pk);
+                }
+                tmem_wait_st();
+                l = l * alpha + (ls2.x + ls2.y);
+                // V rows at or past the sequence end (tail slots) must not reach the MMA
+                if ((u.kt0 + kt) * kN + kN > u.seq_len) {
+                    const int st = gt % kStages;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&s.v_full[st], (gt / kStages) & 1));
+                    if (!ok) break;
+                    if ((u.kt0 + kt) * kN + r >= u.seq_len) {
+                        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            *reinterpret_cast<uint4 *>(s.v[st] + h2 * kHalfBytes + r * 128 + i * 16) = z;
+                    }
+                    fence_proxy_async_smem();  // the zeroed V rows before the tensor core reads them
+                }
+                tc_fence_before();
+                mbar_arrive(&s.p_ready[gt % 3]);
+            }
+            if (ok && u.n_kt > 0)
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(gt - 1) % 3], ((gt - 1) / 3) & 1));
+            float l_other = 0.f;
+            if (ok) ok = exchange(l, l_other);
+            if (!ok) {
+                set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_SOFTMAX);
+            } else {
+                // every lane loads (warp-collective); only rows of real queries store.
+                // A row with no key in this split (only with splits > 1) writes a zero
+                // partial and lse = -inf; O was not written for it.
+                tc_fence_after();
+                const float lsum = l + l_other;
+                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                const int64_t orow = (int64_t)(u.q0 + r) * prm.hq + u.h;
+                if (prm.splits > 1) {
+                    const int64_t rows = (int64_t)prm.plan.queries * prm.hq;
+                    float *dst = prm.ws_o + ((int64_t)u.split * rows + orow) * kD + col0;
+#pragma unroll 1
+                    for (int c = 0; c < 64; c += 16) {
+                        uint32_t v[16];
+                        if (u.n_kt > 0) {
+                            tmem_ld16(tmem_o + lane_off + col0 + c, v);
+                            tmem_wait_ld();
+                        }
+                        if (r < u.nq) {
+#pragma unroll
+                            for (int i = 0; i < 16; i += 4)
+                                *reinterpret_cast<float4 *>(dst + c + i) =
+                                    lsum > 0.f ? make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
+                                                             __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+                    if (r < u.nq && h2 == 0)
+                        prm.ws_lse[(int64_t)u.split * rows + orow] =
+                            lsum > 0.f ? (m_ref + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+                } else {
+                T *dst = static_cast<T *>(prm.out) + orow * kD + col0;
 #pragma unroll 1
                 for (int c = 0; c < 64; c += 16) {
                     uint32_t v[16];
                     tmem_ld16(tmem_o + lane_off + col0 + c, v);
                     tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tmem_st16(tmem_o + lane_off + col0 + c, v);
-                }
-                tmem_wait_st();
-            }
-            // P = exp2(s * scale - m_ref) as 16-bit pairs over my S columns (already in
-            // registers); masked keys hold -inf and give 0.  A row whose window has
-            // not started yet still has m_ref = -inf: its weights are all 0.
-            const float2 sc2 = make_float2(prm.scale_log2, prm.scale_log2);
-            const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-            const float2 nm2 = make_float2(-mr, -mr);
-            float2 ls2 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int c = 0; c < 64; c += 32) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float2 x = ffma2(make_float2(__uint_as_float(sv[c + 2 * i]), __uint_as_float(sv[c + 2 * i + 1])),
-                                           sc2, nm2);
-                    const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-                    ls2 = fadd2(ls2, pp);
-                    pk[i] = pack2<T>(pp.x, pp.y);
-                }
-                tmem_st16(tmem_s(sb) + lane_off + (col0 + c) / 2, pk);
-            }
-            tmem_wait_st();
-            l = l * alpha + (ls2.x + ls2.y);
-            // V rows at or past the sequence end (tail slots) must not reach the MMA
-            if ((kt0 + kt) * kN + kN > seq_len) {
-                const int st = kt % kStages;
-                ok = __all_sync(0xffffffffu, mbar_wait(&s.v_full[st], (kt / kStages) & 1));
-                if (!ok) break;
-                if ((kt0 + kt) * kN + r >= seq_len) {
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        *reinterpret_cast<uint4 *>(s.v[st] + h2 * kHalfBytes + r * 128 + i * 16) = z;
-                }
-                fence_proxy_async_smem();  // the zeroed V rows before the tensor core reads them
-            }
-            tc_fence_before();
-            mbar_arrive(&s.p_ready[kt % 3]);
-        }
-        if (ok && n_kt > 0)
-            ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) % 3], ((n_kt - 1) / 3) & 1));
-        float l_other = 0.f;
-        if (ok) ok = exchange(l, l_other);
-        if (!ok) {
-            set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_SOFTMAX);
-        } else {
-            // every lane loads (warp-collective); only rows of real queries store.
-            // A row with no key in this split (only with splits > 1) writes a zero
-            // partial and lse = -inf; O was not written for it.
-            tc_fence_after();
-            const float lsum = l + l_other;
-            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            const int64_t orow = (int64_t)(q0 + r) * prm.hq + h;
-            if (prm.splits > 1) {
-                const int64_t rows = (int64_t)prm.plan.queries * prm.hq;
-                float *dst = prm.ws_o + ((int64_t)split * rows + orow) * kD + col0;
-#pragma unroll 1
-                for (int c = 0; c < 64; c += 16) {
-                    uint32_t v[16];
-                    if (n_kt > 0) {
-                        tmem_ld16(tmem_o + lane_off + col0 + c, v);
-                        tmem_wait_ld();
-                    }
-                    if (r < nq) {
-#pragma unroll
-                        for (int i = 0; i < 16; i += 4)
-                            *reinterpret_cast<float4 *>(dst + c + i) =
-                                lsum > 0.f ? make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
-                                                         __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv)
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    uint4 w0, w1;
+                    w0.x = pack2<T>(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
+                    w0.y = pack2<T>(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+                    w0.z = pack2<T>(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
+                    w0.w = pack2<T>(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
+                    w1.x = pack2<T>(__uint_as_float(v[8]) * inv, __uint_as_float(v[9]) * inv);
+                    w1.y = pack2<T>(__uint_as_float(v[10]) * inv, __uint_as_float(v[11]) * inv);
+                    w1.z = pack2<T>(__uint_as_float(v[12]) * inv, __uint_as_float(v[13]) * inv);
+                    w1.w = pack2<T>(__uint_as_float(v[14]) * inv, __uint_as_float(v[15]) * inv);
+                    if (r < u.nq) {
+                        reinterpret_cast<uint4 *>(dst + c)[0] = w0;
+                        reinterpret_cast<uint4 *>(dst + c)[1] = w1;
                     }
                 }
-                if (r < nq && h2 == 0)
-                    prm.ws_lse[(int64_t)split * rows + orow] =
-                        lsum > 0.f ? (m_ref + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
-            } else {
-            T *dst = static_cast<T *>(prm.out) + orow * kD + col0;
-#pragma unroll 1
-            for (int c = 0; c < 64; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem_o + lane_off + col0 + c, v);
-                tmem_wait_ld();
-                uint4 w0, w1;
-                w0.x = pack2<T>(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
-                w0.y = pack2<T>(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
-                w0.z = pack2<T>(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
-                w0.w = pack2<T>(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
-                w1.x = pack2<T>(__uint_as_float(v[8]) * inv, __uint_as_float(v[9]) * inv);
-                w1.y = pack2<T>(__uint_as_float(v[10]) * inv, __uint_as_float(v[11]) * inv);
-                w1.z = pack2<T>(__uint_as_float(v[12]) * inv, __uint_as_float(v[13]) * inv);
-                w1.w = pack2<T>(__uint_as_float(v[14]) * inv, __uint_as_float(v[15]) * inv);
-                if (r < nq) {
-                    reinterpret_cast<uint4 *>(dst + c)[0] = w0;
-                    reinterpret_cast<uint4 *>(dst + c)[1] = w1;
                 }
-            }
+                // O of this unit has been read: the next unit's first P.V may overwrite it
+                tc_fence_before();
+                mbar_arrive(&s.o_free);
             }
         }
     }
@@ -526,8 +582,8 @@ cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {
     // blocks: block = tile * Hq + head, and the group size divides Hq).
     const int group = a.hq / a.hkv;
     const unsigned csize = group % 2 == 0 ? 2u : 1u;
+    const int units = a.plan.n_tiles * a.splits * a.hq / (int)csize;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(a.plan.n_tiles * a.splits * a.hq));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = st;
@@ -538,25 +594,38 @@ cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // Persistent grid: no more clusters than can be resident at once (each
+    // walks its share of the units), so none waits for another to finish.
+    auto launch = [&](auto kernel, int &resident, bool &configured) -> cudaError_t {
+        if (!configured) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+            if (e != cudaSuccess) return e;
+            int clusters = 0;
+            cfg.gridDim = dim3(csize * (unsigned)units);
+            e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+            if (e != cudaSuccess || clusters < 1) {
+                int dev = 0, sms = 0;
+                cudaGetLastError();
+                if (cudaGetDevice(&dev) != cudaSuccess ||
+                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                    return cudaErrorInvalidValue;
+                clusters = sms / (int)csize;
+            }
+            resident = clusters > 0 ? clusters : 1;
+            configured = true;
+        }
+        cfg.gridDim = dim3(csize * (unsigned)(units < resident ? units : resident));
+        return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, prm);
+    };
     cudaError_t e;
     if (bf16) {
-        static bool done = false;
-        if (!done) {
-            e = cudaFuncSetAttribute(prefill_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kSmemBytes);
-            if (e != cudaSuccess) return e;
-            done = true;
-        }
-        e = cudaLaunchKernelEx(&cfg, prefill_kernel<__nv_bfloat16>, tq, tk, tv, prm);
+        static int resident[3] = {0, 0, 0};
+        static bool configured[3] = {false, false, false};
+        e = launch(prefill_kernel<__nv_bfloat16>, resident[csize], configured[csize]);
     } else {
-        static bool done = false;
-        if (!done) {
-            e = cudaFuncSetAttribute(prefill_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kSmemBytes);
-            if (e != cudaSuccess) return e;
-            done = true;
-        }
-        e = cudaLaunchKernelEx(&cfg, prefill_kernel<__half>, tq, tk, tv, prm);
+        static int resident[3] = {0, 0, 0};
+        static bool configured[3] = {false, false, false};
+        e = launch(prefill_kernel<__half>, resident[csize], configured[csize]);
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
