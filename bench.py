@@ -230,32 +230,42 @@ class DecodeStep:
 
 
 def time_step(step: DecodeStep, steps: int, warmup: int, world: int, device, sampler=None):
+    """K steps back to back between two events (nothing recorded between the
+    kernels, so each launch may overlap the tail of the one before it), then
+    a separate pass of up to 200 steps with events around the append, the
+    attention call and its main kernel for the per-kernel breakdown."""
     for _ in range(warmup):
         step.store()
         step.attend()
     torch.cuda.synchronize(device)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
-    for e in evs:              # create the CUDA events before timing
-        for ev in e:
-            ev.record()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(device)
     if sampler:
         sampler.start()
     t0.record()
-    for i in range(steps):
+    for _ in range(steps):
+        step.store()
+        step.attend()
+    t1.record()
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop() if sampler else None
+    barrier(world)
+    total = t0.elapsed_time(t1)
+    nb = min(steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(nb)]
+    for e in evs:              # create the CUDA events before use
+        for ev in e:
+            ev.record()
+    torch.cuda.synchronize(device)
+    for i in range(nb):
         evs[i][0].record()
         step.store()
         evs[i][1].record()
         step.pka.time_next_kernel(evs[i][3], evs[i][4])   # brackets the main attention kernel
         step.attend()
         evs[i][2].record()
-    t1.record()
     torch.cuda.synchronize(device)
-    clocks = sampler.stop() if sampler else None
-    barrier(world)
-    total = t0.elapsed_time(t1)
     store_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     kern_ms = [e[3].elapsed_time(e[4]) for e in evs]

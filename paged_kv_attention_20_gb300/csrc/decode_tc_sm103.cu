@@ -115,6 +115,7 @@ template <typename T, int CW>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      AttnArgs a, int use_list, TcParams tp) {
+    griddep_wait();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if ((smem_u32(smem_raw) & 1023u) != 0u) {
         if (threadIdx.x == 0) atomicCAS(a.status, 0, PA_DEVICE_LAYOUT);
@@ -368,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         if (ok && n_kt > 0)
             ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) % kSB], ((n_kt - 1) / kSB) & 1));
+        griddep_launch();         // the tiles are done; only the merge of the copies remains
         const int64_t rows = (int64_t)a.plan.queries * a.hq;
         const int64_t orow0 = (int64_t)qi * a.hq + (int64_t)kvh * G;      // output row of head 0
         // every softmax thread reaches the merge barriers, whatever happened above
@@ -434,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
         }
     }
+    griddep_launch();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -462,7 +465,8 @@ cudaError_t launch_cw(const AttnArgs &a, int items, int use_list, const CUtensor
         configured = true;
     }
     const dim3 grid((unsigned)((int64_t)items * a.splits * a.hkv));
-    decode_tc_kernel<T, CW><<<grid, kThreads, kSmemBytes, st>>>(tk, tv, a, use_list, tp);
+    cudaError_t e = launch_pdl(decode_tc_kernel<T, CW>, grid, dim3(kThreads), kSmemBytes, st, tk, tv, a, use_list, tp);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

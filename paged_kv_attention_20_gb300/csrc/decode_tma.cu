@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
                                                          const __grid_constant__ CUtensorMap tm_v, AttnArgs a,
                                                          int use_list, TmaParams tp) {
     using C = Cfg<D, GH>;
+    griddep_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -333,6 +334,7 @@ __global__ void __launch_bounds__(128) decode_tma_kernel(const __grid_constant__
     }
     if (!ok) atomicCAS(a.status, 0, PA_DEVICE_TIMEOUT_TMA);
 
+    griddep_launch();
     // Merge the four warp states: M = max_w m_w, O = sum_w 2^(m_w-M) acc_w / sum_w 2^(m_w-M) l_w.
     __syncthreads();  // every ring is drained (each warp consumed all its tiles)
     float *mo = reinterpret_cast<float *>(smem);                    // [NW][GH][D] partial O
@@ -403,7 +405,8 @@ cudaError_t launch_t(const AttnArgs &a, int items, int use_list, const CUtensorM
     TmaParams p = tp;
     p.groups = (a.hq / a.hkv) / GH;
     const dim3 grid((unsigned)((int64_t)items * a.splits * a.hkv * p.groups));
-    decode_tma_kernel<T, D, GH><<<grid, 128, C::SMEM, st>>>(tk, tv, a, use_list, p);
+    cudaError_t e = launch_pdl(decode_tma_kernel<T, D, GH>, grid, dim3(128), C::SMEM, st, tk, tv, a, use_list, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -121,6 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
                const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_kp,
                MlaParams prm) {
+    griddep_wait();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if ((smem_u32(smem_raw) & 1023u) != 0u) {
         if (threadIdx.x == 0) atomicCAS(prm.status, 0, PA_DEVICE_LAYOUT);
@@ -428,6 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 prm.ws_lse[(int64_t)split * rows + orow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
         }
     }
+    griddep_launch();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -500,7 +502,8 @@ cudaError_t launch_mla(const AttnArgs &a, bool use_list, cudaStream_t st) {
             if (e != cudaSuccess) return e;
             cfg = true;
         }
-        mla_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(tq, tqp, tlat, tkp, prm);
+        e = launch_pdl(mla_kernel<__nv_bfloat16>, grid, dim3(kThreads), kSmemBytes, st, tq, tqp, tlat, tkp, prm);
+        if (e != cudaSuccess) return e;
     } else {
         static bool cfg = false;
         if (!cfg) {
@@ -508,7 +511,8 @@ cudaError_t launch_mla(const AttnArgs &a, bool use_list, cudaStream_t st) {
             if (e != cudaSuccess) return e;
             cfg = true;
         }
-        mla_kernel<__half><<<grid, kThreads, kSmemBytes, st>>>(tq, tqp, tlat, tkp, prm);
+        e = launch_pdl(mla_kernel<__half>, grid, dim3(kThreads), kSmemBytes, st, tq, tqp, tlat, tkp, prm);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -115,6 +115,34 @@ cudaError_t read_device_status(int32_t *code, bool clear);
 // Device address of the status word on the current device (cached per device).
 int32_t *device_status_ptr();
 
+#ifdef __CUDACC__
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with it allowed, so its CTAs may be scheduled before the kernel ahead of it
+// in the stream has finished; each kernel therefore calls griddep_wait()
+// before its first global-memory access (it returns once the preceding grid
+// has completed and its writes are visible; without the launch attribute it
+// returns at once).  A kernel calls griddep_launch() once its remaining work
+// no longer needs SM room that a waiting dependent could take.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+#endif
+
 }  // namespace pa
 
 // Record `msg` as this thread's last error and return `status`.

@@ -122,6 +122,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, PrefillParams prm) {
+    griddep_wait();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if ((smem_u32(smem_raw) & 1023u) != 0u) {
         if (threadIdx.x == 0) atomicCAS(prm.status, 0, PA_DEVICE_LAYOUT);
@@ -532,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
+    griddep_launch();
     tc_fence_before();
     cluster_barrier();
     if (warp == 0) {
@@ -587,13 +589,15 @@ cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // programmatic dependent launch
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     // Persistent grid: no more clusters than can be resident at once (each
     // walks its share of the units), so none waits for another to finish.
     auto launch = [&](auto kernel, int &resident, bool &configured) -> cudaError_t {

@@ -24,6 +24,8 @@ __global__ void kv_store_kernel(PlanView plan, const U *__restrict__ new_k, cons
                                 U *__restrict__ kc, U *__restrict__ vc, int heads, int uk, int uv,
                                 int64_t total) {
     // One work unit = one U-sized piece of one row; K pieces then V pieces per (query, head).
+    griddep_wait();
+    griddep_launch();
     const int per_row = uk + uv;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -54,17 +56,18 @@ cudaError_t launch_kv_store(const PlanView &plan, const void *new_k, const void 
     int64_t blocks = (total + threads - 1) / threads;
     if (blocks > 152 * 32) blocks = 152 * 32;
     if (blocks < 1) blocks = 1;
+    const dim3 grid((unsigned)blocks), block(threads);
+    cudaError_t e;
     if (unit == 16)
-        kv_store_kernel<uint4><<<(unsigned)blocks, threads, 0, st>>>(
-            plan, (const uint4 *)new_k, (const uint4 *)new_v, (uint4 *)k_cache, (uint4 *)v_cache, heads, uk, uv, total);
+        e = launch_pdl(kv_store_kernel<uint4>, grid, block, 0, st, plan, (const uint4 *)new_k, (const uint4 *)new_v,
+                       (uint4 *)k_cache, (uint4 *)v_cache, heads, uk, uv, total);
     else if (unit == 4)
-        kv_store_kernel<uint32_t><<<(unsigned)blocks, threads, 0, st>>>(
-            plan, (const uint32_t *)new_k, (const uint32_t *)new_v, (uint32_t *)k_cache, (uint32_t *)v_cache, heads,
-            uk, uv, total);
+        e = launch_pdl(kv_store_kernel<uint32_t>, grid, block, 0, st, plan, (const uint32_t *)new_k,
+                       (const uint32_t *)new_v, (uint32_t *)k_cache, (uint32_t *)v_cache, heads, uk, uv, total);
     else
-        kv_store_kernel<uint16_t><<<(unsigned)blocks, threads, 0, st>>>(
-            plan, (const uint16_t *)new_k, (const uint16_t *)new_v, (uint16_t *)k_cache, (uint16_t *)v_cache, heads,
-            uk, uv, total);
+        e = launch_pdl(kv_store_kernel<uint16_t>, grid, block, 0, st, plan, (const uint16_t *)new_k,
+                       (const uint16_t *)new_v, (uint16_t *)k_cache, (uint16_t *)v_cache, heads, uk, uv, total);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -115,6 +118,8 @@ template <int VEC> __device__ __forceinline__ void load_vec(const float *p, floa
 
 template <typename T, int VEC>
 __global__ void __launch_bounds__(256) merge_kernel(AttnArgs a, int use_list, int nrows) {
+    griddep_wait();
+    griddep_launch();
     const int wid = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (wid >= nrows) return;
@@ -154,12 +159,13 @@ __global__ void __launch_bounds__(256) merge_kernel(AttnArgs a, int use_list, in
     }
 }
 
-template <int VEC> void launch_merge_vec(const AttnArgs &a, bool use_list, int nrows, cudaStream_t st) {
-    const unsigned blocks = (unsigned)((nrows + 7) / 8);
+template <int VEC> cudaError_t launch_merge_vec(const AttnArgs &a, bool use_list, int nrows, cudaStream_t st) {
+    const dim3 grid((unsigned)((nrows + 7) / 8)), block(256);
+    const int ul = use_list ? 1 : 0;
     switch (a.dtype) {
-        case PA_F32: merge_kernel<float, VEC><<<blocks, 256, 0, st>>>(a, use_list, nrows); break;
-        case PA_F16: merge_kernel<__half, VEC><<<blocks, 256, 0, st>>>(a, use_list, nrows); break;
-        default: merge_kernel<__nv_bfloat16, VEC><<<blocks, 256, 0, st>>>(a, use_list, nrows); break;
+        case PA_F32: return launch_pdl(merge_kernel<float, VEC>, grid, block, 0, st, a, ul, nrows);
+        case PA_F16: return launch_pdl(merge_kernel<__half, VEC>, grid, block, 0, st, a, ul, nrows);
+        default: return launch_pdl(merge_kernel<__nv_bfloat16, VEC>, grid, block, 0, st, a, ul, nrows);
     }
 }
 
@@ -171,12 +177,14 @@ cudaError_t launch_merge(const AttnArgs &a, bool use_list, cudaStream_t st) {
     // takes 4-wide stores only when its base allows them
     const uintptr_t ob = reinterpret_cast<uintptr_t>(a.out);
     const uintptr_t esz = a.dtype == PA_F32 ? 4 : 2;
+    cudaError_t e;
     if (a.dv % 4 == 0 && ob % (4 * esz) == 0)
-        launch_merge_vec<4>(a, use_list, nrows, st);
+        e = launch_merge_vec<4>(a, use_list, nrows, st);
     else if (a.dv % 2 == 0)
-        launch_merge_vec<2>(a, use_list, nrows, st);
+        e = launch_merge_vec<2>(a, use_list, nrows, st);
     else
-        launch_merge_vec<1>(a, use_list, nrows, st);
+        e = launch_merge_vec<1>(a, use_list, nrows, st);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -185,6 +193,8 @@ cudaError_t launch_merge(const AttnArgs &a, bool use_list, cudaStream_t st) {
 // it.  A position the table does not map (past the row, or a negative or
 // out-of-pool entry) leaves the query unchanged and records PA_DEVICE_RANGE.
 __global__ void plan_advance_kernel(PlanView plan, int32_t *status) {
+    griddep_wait();           // the previous kernel may still read the plan
+    griddep_launch();
     const int q = blockIdx.x * blockDim.x + threadIdx.x;
     if (q >= plan.queries) return;
     int4 *meta = const_cast<int4 *>(plan.qmeta) + q;
@@ -205,7 +215,9 @@ __global__ void plan_advance_kernel(PlanView plan, int32_t *status) {
 
 cudaError_t launch_plan_advance(const PlanView &plan, int32_t *status, cudaStream_t st) {
     const int threads = 128;
-    plan_advance_kernel<<<(plan.queries + threads - 1) / threads, threads, 0, st>>>(plan, status);
+    cudaError_t e = launch_pdl(plan_advance_kernel, dim3((unsigned)((plan.queries + threads - 1) / threads)),
+                               dim3(threads), 0, st, plan, status);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
