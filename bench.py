@@ -415,18 +415,22 @@ def _split_sweep(c3, name, desc, counts, device, warmup, steps, hbm):
         for _ in range(warmup):
             st.attend()
         torch.cuda.synchronize(device)
-        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for a, b in kev:
-            a.record()
-            b.record()
+        # calls back to back (nothing between them), then the main kernel alone
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for i in range(steps):
-            st.pka.time_next_kernel(*kev[i])
+        for _ in range(steps):
             st.attend()
         e1.record()
         torch.cuda.synchronize(device)
         ms = e0.elapsed_time(e1) / steps
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in kev:
+            a.record()
+            b.record()
+        for i in range(steps):
+            st.pka.time_next_kernel(*kev[i])
+            st.attend()
+        torch.cuda.synchronize(device)
         kms = statistics.mean(a.elapsed_time(b) for a, b in kev)
         sweep["heuristic" if s is None else str(s)] = {"splits": st.splits, "ms": ms,
                                                         "kv_gbs": kv_bytes(c3) / ms / 1e6, "kernel_ms": kms,
