@@ -259,13 +259,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // at chunk c ^ (row & 7)); each copy holds the group's heads, rows
             // past G in a copy are zero
             const T *qsrc = static_cast<const T *>(a.q) + ((int64_t)qi * a.hq + (int64_t)kvh * G) * kD;
-            for (int idx = tid; idx < kM * 16; idx += 128) {
-                const int row = idx >> 4, c = idx & 15;
-                const int hr = row % R;
-                uint4 val = make_uint4(0, 0, 0, 0);
-                if (hr < G) val = reinterpret_cast<const uint4 *>(qsrc + (int64_t)hr * kD)[c];
-                const int blk = c >> 3, cc = c & 7;
-                *reinterpret_cast<uint4 *>(s.q[blk] + row * 128 + ((cc ^ (row & 7)) * 16)) = val;
+            // thread tid moves chunk tid % 16 of rows tid / 16 + 8j: every load in
+            // flight before the first store (stores to shared memory would order them)
+            const int c = tid & 15, blk = c >> 3, cc = c & 7;
+            uint4 val[kM / 8];
+#pragma unroll
+            for (int j = 0; j < kM / 8; ++j) {
+                const int hr = ((tid >> 4) + 8 * j) % R;
+                val[j] = hr < G ? reinterpret_cast<const uint4 *>(qsrc + (int64_t)hr * kD)[c] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < kM / 8; ++j) {
+                const int row = (tid >> 4) + 8 * j;
+                *reinterpret_cast<uint4 *>(s.q[blk] + row * 128 + ((cc ^ (row & 7)) * 16)) = val[j];
             }
             fence_proxy_async_smem();       // generic stores before the tensor core reads them
             mbar_arrive(&s.q_ready);
