@@ -22,6 +22,10 @@
 // the tensor core do 128/G times the useful work, which still leaves it idle
 // most of a tile's HBM time; the kernel stays bound by the KV bytes.
 //
+// The kernel is persistent: one CTA per SM walks units (query, split, KV
+// head), and the K/V ring streams from one unit into the next (one CTA per
+// unit spent ~5.6 µs of every ~50 µs unit starting up and draining).
+//
 // Roles: warps 0-3 softmax/epilogue (thread r = MMA row r, TMEM lane r), warp 4
 // TMA producer (128-key tiles of K and V, three stages; the lanes of the warp
 // issue the boxes of a tile, so its page lookups run in parallel), warp 5 MMA
@@ -70,7 +74,9 @@ struct Smem {
     uint64_t s_full[kSB];                // S of tile kt in TMEM buffer kt % kSB
     uint64_t p_ready[kSB];               // P of tile kt written by every softmax thread -> p_ready[kt % kSB]
     uint64_t o_done[kSB];                // P.V of tile kt done -> o_done[kt % kSB]
-    uint64_t q_ready;                    // Q rows stored by the softmax threads
+    uint64_t q_ready;                    // Q rows of the CTA's current unit stored (phase = unit parity)
+    uint64_t o_free;                     // the softmax warps have read O of the unit
+    float ml[2 * kM];                    // per row (m, l) of the unit, for the merge of the copies
     uint32_t tmem_base;
 };
 
@@ -124,27 +130,50 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     Smem &s = *reinterpret_cast<Smem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = tp.group;
-
-    // Flattened grid, item slowest (the plan lists decode items longest first),
-    // then split, then KV head.
-    const int kvh = blockIdx.x % a.hkv;
-    const int rest = blockIdx.x / a.hkv;
-    const int split = rest % a.splits;
-    const int item = rest / a.splits;
-    const int qi = use_list ? a.plan.decode[item] : item;
-    const int4 meta = a.plan.qmeta[qi];
-    const int seq = meta.x, pos = meta.y;
     const int ps = a.plan.page_size;
-    const int seq_len = a.plan.seq_lens[seq];
-    int64_t lo, hi;
-    visible_range(pos, seq_len, a.causal, a.window, lo, hi);
-    int64_t j0, j1;
-    split_bounds(lo, hi, a.splits, split, ps, j0, j1);
-    // Tiles start on a TMA box boundary (no box crosses a page); keys of the
-    // first tile below j0 (window or split start) are masked.
-    const int64_t jb = j0 < j1 ? j0 / tp.box_rows * tp.box_rows : j0;
-    const int n_kt = (int)((j1 - jb + kN - 1) / kN);
-    const int32_t *trow = a.plan.table + (int64_t)seq * a.plan.width;
+
+    // Persistent: each CTA walks its share of the units (item, split, KV head)
+    // in that nesting, item slowest (the plan lists decode items longest
+    // first).  Ring stages and S buffers follow one tile counter that runs on
+    // across units, so the producer streams the next unit's tiles while the
+    // current one finishes.
+    const int items = use_list ? a.plan.n_decode : a.plan.queries;
+    const int units = items * a.splits * a.hkv;
+    struct Unit {
+        int kvh, split, qi, seq_len, n_kt;
+        int64_t j0, j1, jb;
+        const int32_t *trow;
+    };
+    auto unit_at = [&](int u) -> Unit {
+        Unit x;
+        x.kvh = u % a.hkv;
+        const int rest = u / a.hkv;
+        x.split = rest % a.splits;
+        const int item = rest / a.splits;
+        x.qi = use_list ? a.plan.decode[item] : item;
+        const int4 meta = a.plan.qmeta[x.qi];
+        x.seq_len = a.plan.seq_lens[meta.x];
+        int64_t lo, hi;
+        visible_range(meta.y, x.seq_len, a.causal, a.window, lo, hi);
+        split_bounds(lo, hi, a.splits, x.split, ps, x.j0, x.j1);
+        // Tiles start on a TMA box boundary (no box crosses a page); keys of the
+        // first tile below j0 (window or split start) are masked.
+        x.jb = x.j0 < x.j1 ? x.j0 / tp.box_rows * tp.box_rows : x.j0;
+        x.n_kt = (int)((x.j1 - x.jb + kN - 1) / kN);
+        x.trow = a.plan.table + (int64_t)meta.x * a.plan.width;
+        return x;
+    };
+
+    // The CTA's i-th unit: round i of grid-sized rounds, taken in serpentine
+    // order (odd rounds from the last CTA down), so with units sorted by
+    // decreasing size the CTAs' totals even out.  The last round may be
+    // partial: a CTA whose slot in it lies past the end has no i-th unit.
+    auto unit_of = [&](int i) -> int {
+        const int g = (int)gridDim.x, b = (int)blockIdx.x;
+        const int slot = (i & 1) ? g - 1 - b : b;
+        const int u = i * g + slot;
+        return (i * g < units && u < units) ? u : units;
+    };
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -157,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             mbar_init(&s.o_done[i], 1);
         }
         mbar_init(&s.q_ready, 128);
+        mbar_init(&s.o_free, 128);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -178,66 +208,86 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
         }
-        const int used_pages = (seq_len + ps - 1) >> tp.ps_shift;
         const int oob_row = a.plan.pages * ps;        // past the cache: TMA zero fill
         const int nb = kN / tp.box_rows;
-        for (int kt = 0; kt < n_kt; ++kt) {
-            const int st = kt % kStages;
-            if (kt >= kStages && !__all_sync(0xffffffffu, mbar_wait(&s.kv_empty[st], ((kt / kStages) - 1) & 1))) {
-                if (lane == 0) atomicCAS(a.status, 0, PA_DEVICE_TIMEOUT_TMA);
-                break;
-            }
-            if (lane == 0) mbar_arrive_expect_tx(&s.kv_full[st], 4u * kBlk);
-            __syncwarp();
-            const int64_t jt = jb + (int64_t)kt * kN;
-            for (int bi = lane; bi < nb; bi += 32) {
-                const int b = bi * tp.box_rows;
-                const int64_t j = jt + b;
-                const int64_t lp = j >> tp.ps_shift;
-                const int row = lp < used_pages ? trow[lp] * ps + (int)(j & (ps - 1)) : oob_row;
-                for (int blk = 0; blk < 2; ++blk) {
-                    tma_load_3d(s.k[st][blk] + b * 128, &tm_k, blk * 64, kvh, row, &s.kv_full[st]);
-                    tma_load_3d(s.v[st][blk] + b * 128, &tm_v, blk * 64, kvh, row, &s.kv_full[st]);
+        int gt = 0;                                   // tiles streamed so far (all units)
+        bool ok = true;
+        for (int i = 0; ok && unit_of(i) < units; ++i) {
+            const Unit x = unit_at(unit_of(i));
+            const int used_pages = (x.seq_len + ps - 1) >> tp.ps_shift;
+            for (int kt = 0; kt < x.n_kt; ++kt, ++gt) {
+                const int st = gt % kStages;
+                if (gt >= kStages && !__all_sync(0xffffffffu, mbar_wait(&s.kv_empty[st], ((gt / kStages) - 1) & 1))) {
+                    if (lane == 0) atomicCAS(a.status, 0, PA_DEVICE_TIMEOUT_TMA);
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&s.kv_full[st], 4u * kBlk);
+                __syncwarp();
+                const int64_t jt = x.jb + (int64_t)kt * kN;
+                for (int bi = lane; bi < nb; bi += 32) {
+                    const int b = bi * tp.box_rows;
+                    const int64_t j = jt + b;
+                    const int64_t lp = j >> tp.ps_shift;
+                    const int row = lp < used_pages ? x.trow[lp] * ps + (int)(j & (ps - 1)) : oob_row;
+                    for (int blk = 0; blk < 2; ++blk) {
+                        tma_load_3d(s.k[st][blk] + b * 128, &tm_k, blk * 64, x.kvh, row, &s.kv_full[st]);
+                        tma_load_3d(s.v[st][blk] + b * 128, &tm_v, blk * 64, x.kvh, row, &s.kv_full[st]);
+                    }
                 }
             }
         }
     } else if (warp == 5) {
         // ------------------------------------------------------ MMA issuer --
+        // Per tile: P.V of the previous tile first (its stage goes back to the
+        // producer as soon as its own P.V has run), then S of this tile.  The
+        // first P.V of a unit overwrites O, so it waits until the softmax warps
+        // have read O of the previous unit.
         if (lane == 0) {
             const uint32_t idesc_s = idesc_f16(kM, kN, tp.bf16 != 0, false, false);
             const uint32_t idesc_o = idesc_f16(kM, kD, tp.bf16 != 0, false, true);
-            bool ok = mbar_wait(&s.q_ready, 0);
-            auto issue_pv = [&](int kt) -> bool {
-                if (!mbar_wait(&s.p_ready[kt % kSB], (kt / kSB) & 1)) return false;
+            auto issue_pv = [&](int g, bool first) -> bool {     // g: global tile index
+                if (!mbar_wait(&s.p_ready[g % kSB], (g / kSB) & 1)) return false;
                 tc_fence_after();
-                const int st = kt % kStages;
+                const int st = g % kStages;
                 const uint32_t v_addr = smem_u32(s.v[st][0]);
                 for (int ks = 0; ks < kN / 16; ++ks) {
                     const uint64_t b = smem_desc(v_addr + ks * 2048, kBlk, 1024, kLayoutSwizzle128B);
-                    mma_f16_ts(tmem_o, tmem_s(kt % kSB) + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
+                    mma_f16_ts(tmem_o, tmem_s(g % kSB) + ks * 8, b, idesc_o, (!first || ks > 0) ? 1u : 0u);
                 }
-                mma_commit(&s.o_done[kt % kSB]);
+                mma_commit(&s.o_done[g % kSB]);
                 mma_commit(&s.kv_empty[st]);
                 return true;
             };
-            for (int kt = 0; ok && kt < n_kt; ++kt) {
-                const int st = kt % kStages, sb = kt % kSB;
-                // P.V of the previous tile first: its stage is released as soon as
-                // its own P.V has run, not after this tile's data has landed
-                if (kt > 0 && !issue_pv(kt - 1)) { ok = false; break; }
-                if (!mbar_wait(&s.kv_full[st], (kt / kStages) & 1)) { ok = false; break; }
-                // the buffer's previous tile (kt-kSB) must be through its P.V (P lives in it)
-                if (kt >= kSB && !mbar_wait(&s.o_done[sb], ((kt / kSB) - 1) & 1)) { ok = false; break; }
-                tc_fence_after();
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const int blk = ks / 4, k = ks % 4;
-                    const uint64_t qa = smem_desc(smem_u32(s.q[blk]) + k * 32, 16, 1024, kLayoutSwizzle128B);
-                    const uint64_t kb = smem_desc(smem_u32(s.k[st][blk]) + k * 32, 16, 1024, kLayoutSwizzle128B);
-                    mma_f16_ss(tmem_s(sb), qa, kb, idesc_s, ks > 0 ? 1u : 0u);
+            bool ok = true;
+            int gt = 0;
+            for (int i = 0; ok && unit_of(i) < units; ++i) {
+                const Unit x = unit_at(unit_of(i));
+                if (!mbar_wait(&s.q_ready, i & 1)) { ok = false; break; }
+                for (int kt = 0; kt < x.n_kt; ++kt, ++gt) {
+                    if (kt > 0) {
+                        if (kt == 1 && i > 0 && !mbar_wait(&s.o_free, (i - 1) & 1)) { ok = false; break; }
+                        if (!issue_pv(gt - 1, kt == 1)) { ok = false; break; }
+                    }
+                    const int st = gt % kStages, sb = gt % kSB;
+                    if (!mbar_wait(&s.kv_full[st], (gt / kStages) & 1)) { ok = false; break; }
+                    // the buffer's previous tile (gt-kSB) must be through its P.V (P lives in it)
+                    if (gt >= kSB && !mbar_wait(&s.o_done[sb], ((gt / kSB) - 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    for (int ks = 0; ks < kD / 16; ++ks) {
+                        const int blk = ks / 4, k = ks % 4;
+                        const uint64_t qa = smem_desc(smem_u32(s.q[blk]) + k * 32, 16, 1024, kLayoutSwizzle128B);
+                        const uint64_t kb = smem_desc(smem_u32(s.k[st][blk]) + k * 32, 16, 1024, kLayoutSwizzle128B);
+                        mma_f16_ss(tmem_s(sb), qa, kb, idesc_s, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&s.s_full[sb]);
                 }
-                mma_commit(&s.s_full[sb]);
+                if (!ok) break;
+                if (x.n_kt > 0) {
+                    if (x.n_kt == 1 && i > 0 && !mbar_wait(&s.o_free, (i - 1) & 1)) { ok = false; break; }
+                    if (!issue_pv(gt - 1, x.n_kt == 1)) { ok = false; break; }
+                }
             }
-            if (ok && n_kt > 0) ok = issue_pv(n_kt - 1);
             if (!ok) atomicCAS(a.status, 0, PA_DEVICE_TIMEOUT_MMA);
         }
     } else {
@@ -245,201 +295,215 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // Row r belongs to copy r / R of the group (R = 32, 64 or 128 rows per
         // copy, C = 128 / R copies) and is head r % R (a padding row when that
         // is >= G).  Copy k runs its own online softmax over columns
-        // [k*CW, (k+1)*CW) of every tile (CW = 128 / C) and writes P there and
-        // zeros elsewhere, so its O rows collect only those keys; the copies
-        // merge once at the end like split partials.
+        // [k*CW, (k+1)*CW) of every tile and writes P there and zeros elsewhere,
+        // so its O rows collect only those keys; the copies merge at the end of
+        // each unit like split partials, through the Q buffer (S of the unit is
+        // done by then) before the next unit's Q is written there.
         const int r = tid;
         constexpr int R = kM * CW / kN;                  // rows per copy
         constexpr int C = kN / CW;                       // copies
         const int copy = r / R, h = r - copy * R;
         const int c0 = copy * CW;
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        {
-            // Q rows into the two swizzled 64-dim blocks (16-byte chunk c of row
-            // at chunk c ^ (row & 7)); each copy holds the group's heads, rows
-            // past G in a copy are zero
-            const T *qsrc = static_cast<const T *>(a.q) + ((int64_t)qi * a.hq + (int64_t)kvh * G) * kD;
-            // thread tid moves chunk tid % 16 of rows tid / 16 + 8j: every load in
-            // flight before the first store (stores to shared memory would order them)
-            const int c = tid & 15, blk = c >> 3, cc = c & 7;
-            uint4 val[kM / 8];
-#pragma unroll
-            for (int j = 0; j < kM / 8; ++j) {
-                const int hr = ((tid >> 4) + 8 * j) % R;
-                val[j] = hr < G ? reinterpret_cast<const uint4 *>(qsrc + (int64_t)hr * kD)[c] : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int j = 0; j < kM / 8; ++j) {
-                const int row = (tid >> 4) + 8 * j;
-                *reinterpret_cast<uint4 *>(s.q[blk] + row * 128 + ((cc ^ (row & 7)) * 16)) = val[j];
-            }
-            fence_proxy_async_smem();       // generic stores before the tensor core reads them
-            mbar_arrive(&s.q_ready);
-        }
-        float m_ref = -INFINITY, l = 0.f;
+        const int64_t rows = (int64_t)a.plan.queries * a.hq;
         bool ok = true;
+        int gt = 0;                                      // tiles consumed so far (all units)
         float sc[CW];
-        for (int kt = 0; ok && kt < n_kt; ++kt) {
-            const int pb = kt % kSB;
-            const int64_t kbase = jb + (int64_t)kt * kN;
-            const int valid = (int)((j1 - kbase) < kN ? (j1 - kbase) : kN);
-            const int first = (int)(j0 > kbase ? j0 - kbase : 0);
-            ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[pb], (kt / kSB) & 1));
-            if (!ok) break;
-            tc_fence_after();
+        for (int i = 0; ok && unit_of(i) < units; ++i) {
+            const Unit x = unit_at(unit_of(i));
+            {
+                // Q rows into the two swizzled 64-dim blocks (16-byte chunk c of row
+                // at chunk c ^ (row & 7)); each copy holds the group's heads, rows past
+                // G in a copy are zero.  Thread tid moves chunk tid % 16 of rows
+                // tid / 16 + 8j, every load in flight before the first store.
+                const T *qsrc = static_cast<const T *>(a.q) + ((int64_t)x.qi * a.hq + (int64_t)x.kvh * G) * kD;
+                const int c = tid & 15, blk = c >> 3, cc = c & 7;
+                uint4 val[kM / 8];
 #pragma unroll
-            for (int c = 0; c < CW; c += 32) tmem_ld32f(tmem_s(pb) + lane_off + c0 + c, sc + c);
-            tmem_wait_ld();
-            if (valid < kN || first > 0) {
+                for (int j = 0; j < kM / 8; ++j) {
+                    const int hr = ((tid >> 4) + 8 * j) % R;
+                    val[j] = hr < G ? reinterpret_cast<const uint4 *>(qsrc + (int64_t)hr * kD)[c]
+                                    : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
-                for (int c = 0; c < CW; ++c)
-                    if (c0 + c >= valid || c0 + c < first) sc[c] = -INFINITY;
+                for (int j = 0; j < kM / 8; ++j) {
+                    const int row = (tid >> 4) + 8 * j;
+                    *reinterpret_cast<uint4 *>(s.q[blk] + row * 128 + ((cc ^ (row & 7)) * 16)) = val[j];
+                }
+                fence_proxy_async_smem();       // generic stores before the tensor core reads them
+                mbar_arrive(&s.q_ready);
             }
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int c = 0; c < CW; c += 8) {
-                mx[0] = fmax3(mx[0], sc[c], sc[c + 1]);
-                mx[1] = fmax3(mx[1], sc[c + 2], sc[c + 3]);
-                mx[2] = fmax3(mx[2], sc[c + 4], sc[c + 5]);
-                mx[3] = fmax3(mx[3], sc[c + 6], sc[c + 7]);
-            }
-            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * tp.scale_log2;
-            float alpha = 1.f;
-            if (mt > m_ref + kSlack) {
-                alpha = exp2f(m_ref - mt);          // 0 while this copy had seen no key
-                m_ref = mt;
-            }
-            // rescaling O needs the previous P.V finished (rare: the row max moved by > 2^8)
-            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(kt - 1) % kSB], ((kt - 1) / kSB) & 1));
+            float m_ref = -INFINITY, l = 0.f;
+            for (int kt = 0; ok && kt < x.n_kt; ++kt, ++gt) {
+                const int pb = gt % kSB;
+                const int64_t kbase = x.jb + (int64_t)kt * kN;
+                const int valid = (int)((x.j1 - kbase) < kN ? (x.j1 - kbase) : kN);
+                const int first = (int)(x.j0 > kbase ? x.j0 - kbase : 0);
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.s_full[pb], (gt / kSB) & 1));
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < kD; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tmem_o + lane_off + c, v);
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tmem_st16(tmem_o + lane_off + c, v);
+                for (int c = 0; c < CW; c += 32) tmem_ld32f(tmem_s(pb) + lane_off + c0 + c, sc + c);
+                tmem_wait_ld();
+                if (valid < kN || first > 0) {
+#pragma unroll
+                    for (int c = 0; c < CW; ++c)
+                        if (c0 + c >= valid || c0 + c < first) sc[c] = -INFINITY;
+                }
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c = 0; c < CW; c += 8) {
+                    mx[0] = fmax3(mx[0], sc[c], sc[c + 1]);
+                    mx[1] = fmax3(mx[1], sc[c + 2], sc[c + 3]);
+                    mx[2] = fmax3(mx[2], sc[c + 4], sc[c + 5]);
+                    mx[3] = fmax3(mx[3], sc[c + 6], sc[c + 7]);
+                }
+                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * tp.scale_log2;
+                float alpha = 1.f;
+                if (mt > m_ref + kSlack) {
+                    alpha = exp2f(m_ref - mt);          // 0 while this copy had seen no key
+                    m_ref = mt;
+                }
+                // rescaling O needs the previous P.V finished (rare: the row max moved by > 2^8)
+                if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(gt - 1) % kSB], ((gt - 1) / kSB) & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < kD; c += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem_o + lane_off + c, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        tmem_st16(tmem_o + lane_off + c, v);
+                    }
+                    tmem_wait_st();
+                }
+                // P = exp2(s * scale - m_ref) over this copy's columns as 16-bit
+                // pairs; zeros over the other copies' columns.  A copy that has
+                // seen no visible key yet has only -inf scores (P = 0).
+                const float mref = m_ref == -INFINITY ? 0.f : m_ref;
+                const float2 sc2 = make_float2(tp.scale_log2, tp.scale_log2);
+                const float2 nm2 = make_float2(-mref, -mref);
+                const float2 *s2 = reinterpret_cast<const float2 *>(sc);
+                float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int c = 0; c < CW; c += 32) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 xx = ffma2(s2[c / 2 + i], sc2, nm2);
+                        const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+                        ls[i & 1] = fadd2(ls[i & 1], pp);
+                        pk[i] = pack2<T>(pp.x, pp.y);
+                    }
+                    tmem_st16(tmem_s(pb) + lane_off + (c0 + c) / 2, pk);
+                }
+                if (CW < kN) {
+                    uint32_t zero[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) zero[i] = 0u;
+#pragma unroll
+                    for (int c = 0; c < kN; c += 32)
+                        if (c < c0 || c >= c0 + CW) tmem_st16(tmem_s(pb) + lane_off + c / 2, zero);
                 }
                 tmem_wait_st();
-            }
-            // P = exp2(s * scale - m_ref) over this copy's columns as 16-bit
-            // pairs; zeros over the other copies' columns.  A copy that has
-            // seen no visible key yet has only -inf scores (P = 0).
-            const float mref = m_ref == -INFINITY ? 0.f : m_ref;
-            const float2 sc2 = make_float2(tp.scale_log2, tp.scale_log2);
-            const float2 nm2 = make_float2(-mref, -mref);
-            const float2 *s2 = reinterpret_cast<const float2 *>(sc);
-            float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                const float2 lsum = fadd2(ls[0], ls[1]);
+                l = l * alpha + (lsum.x + lsum.y);
+                // value rows past the visible end must not reach P.V (tail slots may hold NaN)
+                if (valid < kN) {
+                    const int st = gt % kStages;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&s.kv_full[st], (gt / kStages) & 1));
+                    if (!ok) break;
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    for (int row = valid + tid; row < kN; row += 128)
 #pragma unroll
-            for (int c = 0; c < CW; c += 32) {
-                uint32_t pk[16];
+                        for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float2 x = ffma2(s2[c / 2 + i], sc2, nm2);
-                    const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-                    ls[i & 1] = fadd2(ls[i & 1], pp);
-                    pk[i] = pack2<T>(pp.x, pp.y);
+                            for (int i = 0; i < 8; ++i)
+                                *reinterpret_cast<uint4 *>(s.v[st][blk] + row * 128 + i * 16) = z;
+                    fence_proxy_async_smem();  // the zeroed rows before the tensor core reads them
                 }
-                tmem_st16(tmem_s(pb) + lane_off + (c0 + c) / 2, pk);
+                tc_fence_before();
+                mbar_arrive(&s.p_ready[pb]);
             }
-            if (CW < kN) {
-                uint32_t zero[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) zero[i] = 0u;
-#pragma unroll
-                for (int c = 0; c < kN; c += 32)
-                    if (c < c0 || c >= c0 + CW) tmem_st16(tmem_s(pb) + lane_off + c / 2, zero);
+            if (ok && x.n_kt > 0)
+                ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(gt - 1) % kSB], ((gt - 1) / kSB) & 1));
+            // every softmax thread reaches the merge barriers, whatever happened above
+            ok = __syncthreads_and_softmax(ok);
+            if (!ok) {
+                atomicCAS(a.status, 0, PA_DEVICE_TIMEOUT_SOFTMAX);
+                break;
             }
-            tmem_wait_st();
-            const float2 lsum = fadd2(ls[0], ls[1]);
-            l = l * alpha + (lsum.x + lsum.y);
-            // value rows past the visible end must not reach P.V (tail slots may hold NaN)
-            if (valid < kN) {
-                const int st = kt % kStages;
-                ok = __all_sync(0xffffffffu, mbar_wait(&s.kv_full[st], (kt / kStages) & 1));
-                if (!ok) break;
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                for (int row = valid + tid; row < kN; row += 128)
-#pragma unroll
-                    for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            *reinterpret_cast<uint4 *>(s.v[st][blk] + row * 128 + i * 16) = z;
-                fence_proxy_async_smem();  // the zeroed rows before the tensor core reads them
-            }
-            tc_fence_before();
-            mbar_arrive(&s.p_ready[pb]);
-        }
-        if (ok && n_kt > 0)
-            ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(n_kt - 1) % kSB], ((n_kt - 1) / kSB) & 1));
-        griddep_launch();         // the tiles are done; only the merge of the copies remains
-        const int64_t rows = (int64_t)a.plan.queries * a.hq;
-        const int64_t orow0 = (int64_t)qi * a.hq + (int64_t)kvh * G;      // output row of head 0
-        // every softmax thread reaches the merge barriers, whatever happened above
-        const bool all_ok = __syncthreads_and_softmax(ok);
-        if (!all_ok) {
-            if (!ok) atomicCAS(a.status, 0, PA_DEVICE_TIMEOUT_SOFTMAX);
-        } else if (n_kt == 0) {
-            // empty split (only with splits > 1): zero partial, lse = -inf
-            if (copy == 0 && h < G && a.splits > 1) {
-                float *dst = a.ws_o + ((int64_t)split * rows + orow0 + h) * kD;
-                for (int c = 0; c < kD; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-                a.ws_lse[(int64_t)split * rows + orow0 + h] = -INFINITY;
-            }
-        } else {
-            // Merge the copies: M = max_k m_k, w_k = 2^(m_k - M), L = sum_k w_k l_k,
-            // O = sum_k w_k O_k / L.  The key stages are free now (every MMA and
-            // TMA load of this CTA has completed), so the merge reuses them.
-            tc_fence_after();
-            float *ml = reinterpret_cast<float *>(s.k[0][0]);          // [128 rows][2]
-            float *ob = ml + 2 * kM;                                     // [C][G][kD] scaled partial O
-            ml[2 * r] = m_ref;
-            ml[2 * r + 1] = l;
-            softmax_bar();
-            float M = -INFINITY;
-            for (int k = 0; k < C; ++k) M = fmaxf(M, ml[2 * (k * R + h)]);
-            float L = 0.f;
-            for (int k = 0; k < C; ++k) {
-                const float mk = ml[2 * (k * R + h)];
-                L += mk == -INFINITY ? 0.f : exp2f(mk - M) * ml[2 * (k * R + h) + 1];
-            }
-            const float wk = (m_ref == -INFINITY || !(L > 0.f)) ? 0.f : exp2f(m_ref - M) / L;
+            const int64_t orow0 = (int64_t)x.qi * a.hq + (int64_t)x.kvh * G;      // output row of head 0
+            if (x.n_kt == 0) {
+                // empty split (only with splits > 1): zero partial, lse = -inf
+                if (copy == 0 && h < G && a.splits > 1) {
+                    float *dst = a.ws_o + ((int64_t)x.split * rows + orow0 + h) * kD;
+                    for (int c = 0; c < kD; c += 4)
+                        *reinterpret_cast<float4 *>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    a.ws_lse[(int64_t)x.split * rows + orow0 + h] = -INFINITY;
+                }
+            } else {
+                // Merge the copies: M = max_k m_k, w_k = 2^(m_k - M), L = sum_k w_k l_k,
+                // O = sum_k w_k O_k / L.
+                tc_fence_after();
+                s.ml[2 * r] = m_ref;
+                s.ml[2 * r + 1] = l;
+                softmax_bar();
+                float M = -INFINITY;
+                for (int k = 0; k < C; ++k) M = fmaxf(M, s.ml[2 * (k * R + h)]);
+                float L = 0.f;
+                for (int k = 0; k < C; ++k) {
+                    const float mk = s.ml[2 * (k * R + h)];
+                    L += mk == -INFINITY ? 0.f : exp2f(mk - M) * s.ml[2 * (k * R + h) + 1];
+                }
+                const float wk = (m_ref == -INFINITY || !(L > 0.f)) ? 0.f : exp2f(m_ref - M) / L;
+                if (copy == 0 && h < G && a.splits > 1)
+                    a.ws_lse[(int64_t)x.split * rows + orow0 + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+                // one pass per 64 output columns; the scaled partials [C][G][64] fill the Q buffer
+                float *ob = reinterpret_cast<float *>(s.q[0]);
 #pragma unroll 1
-            for (int c = 0; c < kD; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem_o + lane_off + c, v);
-                tmem_wait_ld();
-                if (h < G) {
+                for (int half = 0; half < 2; ++half) {
+#pragma unroll 1
+                    for (int c = 0; c < 64; c += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem_o + lane_off + 64 * half + c, v);
+                        tmem_wait_ld();
+                        if (h < G) {
 #pragma unroll
-                    for (int i = 0; i < 16; i += 4)
-                        *reinterpret_cast<float4 *>(ob + ((size_t)copy * G + h) * kD + c + i) =
-                            make_float4(__uint_as_float(v[i]) * wk, __uint_as_float(v[i + 1]) * wk,
-                                        __uint_as_float(v[i + 2]) * wk, __uint_as_float(v[i + 3]) * wk);
+                            for (int i = 0; i < 16; i += 4)
+                                *reinterpret_cast<float4 *>(ob + ((size_t)copy * G + h) * 64 + c + i) =
+                                    make_float4(__uint_as_float(v[i]) * wk, __uint_as_float(v[i + 1]) * wk,
+                                                __uint_as_float(v[i + 2]) * wk, __uint_as_float(v[i + 3]) * wk);
+                        }
+                    }
+                    softmax_bar();
+                    // sum the copies, 4 columns per thread and step
+                    for (int idx = tid; idx < G * 16; idx += 128) {
+                        const int hh = idx >> 4, c = (idx & 15) * 4;
+                        float4 o = *reinterpret_cast<const float4 *>(ob + (size_t)hh * 64 + c);
+                        for (int k = 1; k < C; ++k) {
+                            const float4 y = *reinterpret_cast<const float4 *>(ob + ((size_t)k * G + hh) * 64 + c);
+                            o.x += y.x; o.y += y.y; o.z += y.z; o.w += y.w;
+                        }
+                        const int col = 64 * half + c;
+                        if (a.splits == 1) {
+                            uint2 w;
+                            w.x = pack2<T>(o.x, o.y);
+                            w.y = pack2<T>(o.z, o.w);
+                            *reinterpret_cast<uint2 *>(static_cast<T *>(a.out) + (orow0 + hh) * kD + col) = w;
+                        } else {
+                            *reinterpret_cast<float4 *>(a.ws_o + ((int64_t)x.split * rows + orow0 + hh) * kD + col) = o;
+                        }
+                    }
+                    softmax_bar();      // the Q buffer is read before it is written again
                 }
             }
-            if (copy == 0 && h < G && a.splits > 1)
-                a.ws_lse[(int64_t)split * rows + orow0 + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-            softmax_bar();
-            // sum the copies, 4 columns per thread and step, rows in order
-            for (int idx = tid; idx < G * (kD / 4); idx += 128) {
-                const int hh = idx / (kD / 4), c = (idx % (kD / 4)) * 4;
-                float4 o = *reinterpret_cast<const float4 *>(ob + (size_t)hh * kD + c);
-                for (int k = 1; k < C; ++k) {
-                    const float4 x = *reinterpret_cast<const float4 *>(ob + ((size_t)k * G + hh) * kD + c);
-                    o.x += x.x; o.y += x.y; o.z += x.z; o.w += x.w;
-                }
-                if (a.splits == 1) {
-                    uint2 w;
-                    w.x = pack2<T>(o.x, o.y);
-                    w.y = pack2<T>(o.z, o.w);
-                    *reinterpret_cast<uint2 *>(static_cast<T *>(a.out) + (orow0 + hh) * kD + c) = w;
-                } else {
-                    *reinterpret_cast<float4 *>(a.ws_o + ((int64_t)split * rows + orow0 + hh) * kD + c) = o;
-                }
-            }
+            // O of this unit has been read: the next unit's first P.V may overwrite it
+            tc_fence_before();
+            mbar_arrive(&s.o_free);
         }
     }
     griddep_launch();
@@ -463,14 +527,23 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 template <typename T, int CW>
 cudaError_t launch_cw(const AttnArgs &a, int items, int use_list, const CUtensorMap &tk, const CUtensorMap &tv,
                       const TcParams &tp, cudaStream_t st) {
-    static bool configured = false;
-    if (!configured) {
+    // Persistent grid: as many CTAs as fit on the GPU at once (one per SM).
+    static int resident = 0;
+    if (resident == 0) {
         cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<T, CW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (e != cudaSuccess) return e;
-        configured = true;
+        int per_sm = 0, dev = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tc_kernel<T, CW>, kThreads, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        resident = per_sm * sms > 0 ? per_sm * sms : 1;
     }
-    const dim3 grid((unsigned)((int64_t)items * a.splits * a.hkv));
+    const int64_t units = (int64_t)items * a.splits * a.hkv;
+    const dim3 grid((unsigned)(units < resident ? units : resident));
     cudaError_t e = launch_pdl(decode_tc_kernel<T, CW>, grid, dim3(kThreads), kSmemBytes, st, tk, tv, a, use_list, tp);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

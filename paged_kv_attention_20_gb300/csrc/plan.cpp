@@ -297,6 +297,27 @@ int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32
     int64_t s = (target + blocks - 1) / blocks;
     const int64_t longest = window > 0 ? std::min<int64_t>(plan->max_seq_len, window) : plan->max_seq_len;
     int64_t cap = std::max<int64_t>(1, longest / (4 * (int64_t)plan->page_size));
+    if (group >= 8 && plan->n_tiles == 0) {
+        // Groups of 8+ go to the persistent tensor-core decode: one CTA per SM
+        // walks (query, split, KV head) units in rounds of num_sms.  Aim for about
+        // four rounds and, within a quarter of that, prefer split counts that
+        // fill the last round (a partial round leaves SMs idle at the end).
+        const int64_t n = (int64_t)plan->n_decode * num_kv_heads;
+        const int64_t base = std::max<int64_t>(1, (4 * (int64_t)num_sms + n - 1) / n);
+        double best_fill = -1.0;
+        int64_t best = base;
+        for (int64_t c = std::max<int64_t>(1, base - base / 4); c <= base + base / 4; ++c) {
+            if (c > cap || c > PA_MAX_SPLITS) break;
+            const int64_t units = n * c;
+            const int64_t rounds = (units + num_sms - 1) / num_sms;
+            const double fill = (double)units / (double)(rounds * num_sms);
+            if (fill > best_fill + 1e-9 || (fill > best_fill - 1e-9 && std::llabs(c - base) < std::llabs(best - base))) {
+                best_fill = fill;
+                best = c;
+            }
+        }
+        s = best;
+    }
     s = std::min<int64_t>(s, cap);
     s = std::max<int64_t>(1, std::min<int64_t>(s, PA_MAX_SPLITS));
     return (int32_t)s;

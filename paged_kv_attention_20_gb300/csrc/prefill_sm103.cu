@@ -80,7 +80,6 @@ struct Smem {
                                    // slot n % 2 for exchange n
     uint64_t xa[2][4];             // per slot and lane quarter: both warps' values written
     uint32_t tmem_base;
-    int32_t abort;
 };
 
 // The operand tiles need 1024-byte alignment (128-byte swizzle atoms); the
@@ -104,7 +103,6 @@ struct PrefillParams {
 };
 
 __device__ __forceinline__ void set_timeout(Smem &s, int32_t *status, int code) {
-    atomicExch(&s.abort, 1);
     atomicCAS(status, 0, code);
 }
 
@@ -196,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&s.xa[1][i], 64);
         }
         for (int i = 0; i < 3; ++i) mbar_init(&s.o_done[i], 1);
-        s.abort = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
