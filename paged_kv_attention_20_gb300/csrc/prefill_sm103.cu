@@ -7,8 +7,8 @@
 // sees keys 0..p_i: the cached context plus the chunk's earlier rows.
 //
 // Work unit: (tile of up to 128 consecutive queries, split, query head).  The
-// kernel is persistent: as many clusters as fit on the GPU at once, each
-// walking every n-th unit (heaviest first), so the K/V rings stream on from
+// kernel is persistent: as many clusters as fit on the GPU at once, walking
+// the units (heaviest first) in serpentine rounds, so the K/V rings stream on from
 // one unit into the next, Q of the next unit loads while the last tiles of
 // the current one finish, and a CTA's start-up and teardown are paid once
 // (as one CTA per unit, they cost ~4 µs of every 17-tile unit).  Per unit:
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Smem &s = *reinterpret_cast<Smem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // Persistent: cluster c of C walks units c, c + C, c + 2C, ... of U, a unit
+    // Persistent: each cluster walks its share of the U units, a unit
     // being (query tile, split, csize consecutive query heads) in the order
     // block = (tile * splits + split) * Hq + head; the plan orders tiles by
     // decreasing key count, so the heaviest units go first.  Every role walks
@@ -175,6 +175,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         u.kt0 = (int)(first_j0 / kN);
         u.n_kt = last_j1 > first_j0 ? (int)((last_j1 + kN - 1) / kN) - u.kt0 : 0;
         return u;
+    };
+
+    // The cluster's i-th unit: round i of n_clusters-sized rounds, taken in
+    // serpentine order (odd rounds from the last cluster down), so with units
+    // sorted by decreasing size the clusters' totals even out.  A cluster whose
+    // slot in the last, partial round lies past the end has no i-th unit.
+    auto unit_of = [&](int i) -> int {
+        const int slot = (i & 1) ? n_clusters - 1 - cluster : cluster;
+        const int ui = i * n_clusters + slot;
+        return ui < units ? ui : units;
     };
 
     if (tid == 0) {
@@ -228,8 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int oob_row = prm.plan.pages * ps;          // rows >= this read as zeros
         int gt = 0;                                        // tiles streamed so far (all units)
         bool go = true;
-        for (int ui = cluster, i = 0; go && ui < units; ui += n_clusters, ++i) {
-            const Unit u = unit_at(ui);
+        for (int i = 0; go && unit_of(i) < units; ++i) {
+            const Unit u = unit_at(unit_of(i));
             if (is_k && lane == 0) {
                 if (i > 0 && !mbar_wait(&s.q_empty, (i - 1) & 1)) {
                     set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
@@ -296,8 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 9) {
                 const uint32_t idesc_s = idesc_f16(kM, kN, prm.bf16 != 0, false, false);
                 const uint32_t q_addr = smem_u32(s.q);
-                for (int ui = cluster, i = 0; ok && ui < units; ui += n_clusters, ++i) {
-                    const Unit u = unit_at(ui);
+                for (int i = 0; ok && unit_of(i) < units; ++i) {
+                    const Unit u = unit_at(unit_of(i));
                     if (!mbar_wait(&s.q_full, i & 1)) { ok = false; break; }
                     for (int kt = 0; kt < u.n_kt; ++kt, ++gt) {
                         const int st = gt % kStages, sb = gt % 3;
@@ -323,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 const uint32_t idesc_o = idesc_f16(kM, kD, prm.bf16 != 0, false, true);
-                for (int ui = cluster, i = 0; ok && ui < units; ui += n_clusters, ++i) {
-                    const Unit u = unit_at(ui);
+                for (int i = 0; ok && unit_of(i) < units; ++i) {
+                    const Unit u = unit_at(unit_of(i));
                     if (i > 0 && !mbar_wait(&s.o_free, (i - 1) & 1)) { ok = false; break; }
                     for (int kt = 0; kt < u.n_kt; ++kt, ++gt) {
                         const int st = gt % kStages;
@@ -371,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++xphase;
             return true;
         };
-        for (int ui = cluster; ok && ui < units; ui += n_clusters) {
-            const Unit u = unit_at(ui);
+        for (int i = 0; ok && unit_of(i) < units; ++i) {
+            const Unit u = unit_at(unit_of(i));
             int64_t row_j0 = 0, row_j1 = 0;           // this row's keys in this split: [vis_lo, vis_end)
             if (r < u.nq) row_keys(u, u.pos0 + r, row_j0, row_j1);   // rows past the tile's queries see nothing
             const int vis_lo = (int)row_j0, vis_end = (int)row_j1;
