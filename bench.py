@@ -287,27 +287,33 @@ def soak_clocks(step: DecodeStep, device, seconds=1.0):
 
 
 def e2e_leg(case, device, steps: int, warmup: int):
-    """Same metric through the public API with host buffers, as a serving loop
-    replays a decode step: per step the schedule's device image is staged into
-    pinned memory (Plan.stage), then one CUDA graph replay copies it and the
-    step's inputs (q, new_k, new_v) from pinned memory to the device, appends,
-    attends and copies the result back to pinned memory, and the host waits for
-    it.  Checked once against the same step run call by call."""
-    step = DecodeStep(case, device)
-    host = {k: getattr(case, k).pin_memory() for k in ("q", "new_k", "new_v")}
+    """Same metric through the public API with host buffers, run as a decode
+    loop replays its attention layer: one CUDA graph holds the pinned host-to-
+    device copy of the step's inputs (q, new_k, new_v), pa_plan_advance (every
+    query moves one position on, on the device), the append, the split
+    attention and the device-to-host copy of the output; per step the host
+    replays it and waits.  The case is the GQA decode workload with its pages
+    reserved for the positions the loop reaches; the KV bytes are counted per
+    step as the histories grow.  The last replay is checked against the same
+    attention called directly."""
+    import workloads
+    import paged_kv_attention_20_gb300 as pka
+    total = warmup + steps + 2
+    ctx = [int(n) for n in case.seq_lens]
+    grown = workloads.build_case(case.name + "_loop", case.meta["seed"], [n + total for n in ctx],
+                                 [(i, n - 1) for i, n in enumerate(ctx)], case.hq, case.hkv, case.d, case.dv,
+                                 case.page_size, case.dtype, case.scale)
+    step = DecodeStep(grown, device)
+    host = {k: getattr(grown, k).pin_memory() for k in ("q", "new_k", "new_v")}
     out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    n = step.plan.device_bytes()
-    words = step.plan.words
-    words_host = torch.empty(n, dtype=torch.uint8).pin_memory()
-    step.plan.stage(words_host, words)
-    h2d = sum(t.numel() * t.element_size() for t in host.values()) + n
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * out_host.element_size()
 
     def body():
-        words[:n].copy_(words_host, non_blocking=True)
         step.dc.q.copy_(host["q"], non_blocking=True)
         step.dc.new_k.copy_(host["new_k"], non_blocking=True)
         step.dc.new_v.copy_(host["new_v"], non_blocking=True)
+        pka.paged_attn_plan_advance(step.plan)
         step.store()
         step.attend()
         out_host.copy_(step.out, non_blocking=True)
@@ -315,33 +321,37 @@ def e2e_leg(case, device, steps: int, warmup: int):
     side = torch.cuda.Stream(device)
     side.wait_stream(torch.cuda.current_stream(device))
     with torch.cuda.stream(side):
-        body()                       # kernel attributes are set outside capture
+        body()                       # kernel attributes are set outside capture (first advance)
     torch.cuda.current_stream(device).wait_stream(side)
     torch.cuda.synchronize(device)
-    eager = out_host.clone()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         body()
     stream = torch.cuda.current_stream(device)
 
     def one():
-        step.plan.stage(words_host, words)
         graph.replay()
         stream.synchronize()
 
     for _ in range(warmup):
         one()
+    done = 1 + warmup                # advances so far (the eager step and the warm-up replays)
     t = time.perf_counter()
     for _ in range(steps):
         one()
     dt = time.perf_counter() - t
-    if not torch.equal(out_host, eager) or step.pka.device_status() != 0:
-        raise RuntimeError("graph-replayed step differs from the call-by-call step")
-    return {"value": kv_bytes(case) * steps / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+    # positions during timed step i: ctx - 1 + done + 1 + i; keys seen: that + 1
+    per_tok = grown.hkv * (grown.d + grown.dv) * grown.new_k.element_size()
+    kv = sum((sum(ctx) + len(ctx) * (done + 1 + i)) * per_tok for i in range(steps))
+    last = out_host.clone()
+    step.attend()                    # the same attention on the state the last replay left
+    torch.cuda.synchronize(device)
+    if not torch.equal(step.out.cpu(), last) or pka.device_status() != 0:
+        raise RuntimeError("graph-replayed decode step differs from the direct call")
+    return {"value": kv / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": dt / steps * 1e3,
-            "mode": "per step: Plan.stage into pinned memory, one CUDA graph replay (pinned H2D of the plan "
-                    "image, q, new_k, new_v; paged_kv_store; paged_attn_forward_split; D2H of the output), "
-                    "host wait"}
+            "mode": "per step one CUDA graph replay: pinned H2D of q, new_k, new_v; pa_plan_advance (schedule "
+                    "on the device); paged_kv_store; paged_attn_forward_split; D2H of the output; host wait"}
 
 
 def secondary(device, warmup: int, steps: int, peaks, which):
