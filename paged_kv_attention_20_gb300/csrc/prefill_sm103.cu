@@ -381,8 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++xphase;
             return true;
         };
+        // a unit's parameters come from dependent loads of plan metadata; the
+        // next unit's are fetched before this unit's epilogue, so their latency
+        // overlaps it instead of delaying the next unit's first softmax
+        Unit u = unit_of(0) < units ? unit_at(unit_of(0)) : Unit{};
         for (int i = 0; ok && unit_of(i) < units; ++i) {
-            const Unit u = unit_at(unit_of(i));
             int64_t row_j0 = 0, row_j1 = 0;           // this row's keys in this split: [vis_lo, vis_end)
             if (r < u.nq) row_keys(u, u.pos0 + r, row_j0, row_j1);   // rows past the tile's queries see nothing
             const int vis_lo = (int)row_j0, vis_end = (int)row_j1;
@@ -476,6 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(&s.p_ready[gt % 3]);
             }
+            const bool more = unit_of(i + 1) < units;
+            const Unit nu = more ? unit_at(unit_of(i + 1)) : u;
             if (ok && u.n_kt > 0)
                 ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(gt - 1) % 3], ((gt - 1) / 3) & 1));
             float l_other = 0.f;
@@ -514,11 +519,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             lsum > 0.f ? (m_ref + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
                 } else {
                 T *dst = static_cast<T *>(prm.out) + orow * kD + col0;
-#pragma unroll 1
+                uint32_t vv[64];
+                tmem_ld32(tmem_o + lane_off + col0, vv);          // all 64 columns, one wait
+                tmem_ld32(tmem_o + lane_off + col0 + 32, vv + 32);
+                tmem_wait_ld();
+#pragma unroll
                 for (int c = 0; c < 64; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tmem_o + lane_off + col0 + c, v);
-                    tmem_wait_ld();
+                    const uint32_t *v = vv + c;
                     uint4 w0, w1;
                     w0.x = pack2<T>(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
                     w0.y = pack2<T>(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
@@ -538,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(&s.o_free);
             }
+            u = nu;
         }
     }
     griddep_launch();
