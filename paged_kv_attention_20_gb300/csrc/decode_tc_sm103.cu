@@ -8,22 +8,23 @@
 // over the keys j the query sees.  With G query heads per KV head every KV
 // byte feeds 2*G flops per dim; from G = 8 on, CUDA cores run out of issue
 // slots before HBM runs out of bytes, so the contraction moves to the tensor
-// core.  One CTA per (query, KV head, split) writes the group's G query rows
-// into the 128-row MMA tile C = 128 / R times (R = 32, 64 or 128 rows per
+// core.  For each work unit (query, KV head, split) the group's G query rows
+// go into the 128-row MMA tile C = 128 / R times (R = 32, 64 or 128 rows per
 // copy; rows of a copy past G are zero and their results are never read) and
 // runs, per 128-key tile,
 //   S = Q . K^T   (M = 128, N = 128 keys, K = 128 dims; Q and K in shared memory)
 //   O += P . V    (M = 128, N = 128 dims, K = 128 keys; P in TMEM, V in shared memory)
 // Copy k runs its own online softmax over columns [k*128/C, (k+1)*128/C) of
 // every tile and writes P there and zeros elsewhere, so its O rows collect
-// only those keys; the copies merge once at the end like split partials.  (With
+// only those keys; the copies merge at the end of the unit like split partials,
+// through the Q buffer (the unit's S MMAs are done by then).  (With
 // one copy, G = 8 rows in one warp's TMEM lanes, a single warp had to run the
 // exponentials of every column on one SM sub-partition.)  The padding makes
 // the tensor core do 128/G times the useful work, which still leaves it idle
 // most of a tile's HBM time; the kernel stays bound by the KV bytes.
 //
-// The kernel is persistent: one CTA per SM walks units (query, split, KV
-// head), and the K/V ring streams from one unit into the next (one CTA per
+// The kernel is persistent: one CTA per SM walks the units in serpentine
+// rounds, and the K/V ring streams from one unit into the next (one CTA per
 // unit spent ~5.6 µs of every ~50 µs unit starting up and draining).
 //
 // Roles: warps 0-3 softmax/epilogue (thread r = MMA row r, TMEM lane r), warp 4

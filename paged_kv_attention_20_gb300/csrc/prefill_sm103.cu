@@ -15,7 +15,7 @@
 //   warps 0-7  softmax / O correction / epilogue: query row r (TMEM lane r) is
 //              shared by warps r/32 and r/32+4, each taking 64 of the 128 key
 //              (and output) columns; row maxima and sums cross over shared memory;
-//   warps 8/10 TMA producers: Q once and K tiles (warp 8), V tiles (warp 10)
+//   warps 8/10 TMA producers: Q of each unit and K tiles (warp 8), V tiles (warp 10)
 //              of 128 keys gathered page by page through the block table
 //              (one box per page and 64-column half, 128-byte swizzle), each
 //              through its own ring, so K is released once S is computed;
