@@ -310,30 +310,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         bool ok = true;
         int gt = 0;                                      // tiles consumed so far (all units)
         float sc[CW];
-        for (int i = 0; ok && unit_of(i) < units; ++i) {
-            const Unit x = unit_at(unit_of(i));
-            {
-                // Q rows into the two swizzled 64-dim blocks (16-byte chunk c of row
-                // at chunk c ^ (row & 7)); each copy holds the group's heads, rows past
-                // G in a copy are zero.  Thread tid moves chunk tid % 16 of rows
-                // tid / 16 + 8j, every load in flight before the first store.
-                const T *qsrc = static_cast<const T *>(a.q) + ((int64_t)x.qi * a.hq + (int64_t)x.kvh * G) * kD;
-                const int c = tid & 15, blk = c >> 3, cc = c & 7;
-                uint4 val[kM / 8];
+        // Q rows into the two swizzled 64-dim blocks (16-byte chunk c of row at
+        // chunk c ^ (row & 7)); each copy holds the group's heads, rows past G in
+        // a copy are zero.  Thread tid moves chunk tid % 16 of rows tid / 16 + 8j:
+        // load_q puts every load in flight, store_q writes them to the Q buffer.
+        auto load_q = [&](const Unit &x, uint4 (&val)[kM / 8]) {
+            const T *qsrc = static_cast<const T *>(a.q) + ((int64_t)x.qi * a.hq + (int64_t)x.kvh * G) * kD;
+            const int c = tid & 15;
 #pragma unroll
-                for (int j = 0; j < kM / 8; ++j) {
-                    const int hr = ((tid >> 4) + 8 * j) % R;
-                    val[j] = hr < G ? reinterpret_cast<const uint4 *>(qsrc + (int64_t)hr * kD)[c]
-                                    : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int j = 0; j < kM / 8; ++j) {
-                    const int row = (tid >> 4) + 8 * j;
-                    *reinterpret_cast<uint4 *>(s.q[blk] + row * 128 + ((cc ^ (row & 7)) * 16)) = val[j];
-                }
-                fence_proxy_async_smem();       // generic stores before the tensor core reads them
-                mbar_arrive(&s.q_ready);
+            for (int j = 0; j < kM / 8; ++j) {
+                const int hr = ((tid >> 4) + 8 * j) % R;
+                val[j] = hr < G ? reinterpret_cast<const uint4 *>(qsrc + (int64_t)hr * kD)[c] : make_uint4(0, 0, 0, 0);
             }
+        };
+        auto store_q = [&](const uint4 (&val)[kM / 8]) {
+            const int c = tid & 15, blk = c >> 3, cc = c & 7;
+#pragma unroll
+            for (int j = 0; j < kM / 8; ++j) {
+                const int row = (tid >> 4) + 8 * j;
+                *reinterpret_cast<uint4 *>(s.q[blk] + row * 128 + ((cc ^ (row & 7)) * 16)) = val[j];
+            }
+            fence_proxy_async_smem();       // generic stores before the tensor core reads them
+            mbar_arrive(&s.q_ready);
+        };
+        // The next unit's parameters and (below 128 columns per copy, where the
+        // registers allow) its Q loads are issued before this unit's merge, so
+        // their latency overlaps it.
+        constexpr bool kPrefetchQ = CW < 128;
+        Unit x = unit_of(0) < units ? unit_at(unit_of(0)) : Unit{};
+        if (unit_of(0) < units) {
+            uint4 val[kM / 8];
+            load_q(x, val);
+            store_q(val);
+        }
+        for (int i = 0; ok && unit_of(i) < units; ++i) {
             float m_ref = -INFINITY, l = 0.f;
             for (int kt = 0; ok && kt < x.n_kt; ++kt, ++gt) {
                 const int pb = gt % kSB;
@@ -429,6 +439,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 tc_fence_before();
                 mbar_arrive(&s.p_ready[pb]);
             }
+            const bool more = unit_of(i + 1) < units;
+            const Unit nx = more ? unit_at(unit_of(i + 1)) : x;
+            uint4 qn[kM / 8];
+            if (kPrefetchQ && more) load_q(nx, qn);
             if (ok && x.n_kt > 0)
                 ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(gt - 1) % kSB], ((gt - 1) / kSB) & 1));
             // every softmax thread reaches the merge barriers, whatever happened above
@@ -505,6 +519,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // O of this unit has been read: the next unit's first P.V may overwrite it
             tc_fence_before();
             mbar_arrive(&s.o_free);
+            if (more) {
+                // the merge has read the Q buffer (its last barrier): the next Q goes in
+                if (!kPrefetchQ) load_q(nx, qn);
+                store_q(qn);
+            }
+            x = nx;
         }
     }
     griddep_launch();
