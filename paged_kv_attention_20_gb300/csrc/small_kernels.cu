@@ -128,14 +128,18 @@ __global__ void __launch_bounds__(256) merge_kernel(AttnArgs a, int use_list, in
     const int S = a.splits;
     const int64_t rows = (int64_t)a.plan.queries * a.hq;
     const int64_t row = (int64_t)qi * a.hq + h;
+    // lane l holds the weights of splits l and l + 32 (at most PA_MAX_SPLITS = 64)
     float m = -INFINITY;
     for (int s = lane; s < S; s += 32) m = fmaxf(m, a.ws_lse[s * rows + row]);
     for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float tot = 0.f;
-    for (int s = lane; s < S; s += 32) {
-        const float l = a.ws_lse[s * rows + row];
-        tot += (l == -INFINITY) ? 0.f : __expf(l - m);
+    float wl[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int s = lane + 32 * k;
+        const float l = s < S ? a.ws_lse[s * rows + row] : -INFINITY;
+        wl[k] = l == -INFINITY ? 0.f : __expf(l - m);
     }
+    float tot = wl[0] + wl[1];
     for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
     const float inv = 1.f / tot;
     T *out = static_cast<T *>(a.out) + row * a.dv;
@@ -143,11 +147,11 @@ __global__ void __launch_bounds__(256) merge_kernel(AttnArgs a, int use_list, in
         float acc[VEC];
 #pragma unroll
         for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
-#pragma unroll 4
+        // no branch on empty splits (their weight is 0 and their partial 0), so the
+        // loads of several splits are in flight at once
+#pragma unroll 8
         for (int s = 0; s < S; ++s) {
-            const float l = a.ws_lse[s * rows + row];
-            if (l == -INFINITY) continue;
-            const float ws = __expf(l - m);
+            const float ws = __shfl_sync(0xffffffffu, s < 32 ? wl[0] : wl[1], s & 31);
             float v[VEC];
             load_vec<VEC>(a.ws_o + (s * rows + row) * a.dv + c, v);
 #pragma unroll
