@@ -119,6 +119,24 @@ def test_split_heuristic(built_lib):
     assert pka.paged_attn_split_heuristic(p, 64, 8, num_sms=152, window=4096) <= 4096 // 64
 
 
+def test_split_heuristic_fills_rounds_for_large_groups(built_lib):
+    """Groups of 8+ (persistent tensor-core decode): about four rounds of units, last round nearly full."""
+    lens = [32768, 65536, 98304, 131072]
+    table = np.arange(sum(n // 16 for n in lens), dtype=np.int32)
+    rows, off = [], 0
+    for n in lens:
+        rows.append(np.pad(table[off:off + n // 16], (0, 8192 - n // 16)))
+        off += n // 16
+    p = plan(lens, np.stack(rows), [0, 1, 2, 3], [n - 1 for n in lens], 16, int(table.size))
+    for sms in (152, 148, 100, 132):
+        s = pka.paged_attn_split_heuristic(p, 64, 8, num_sms=sms)
+        units = 4 * 8 * s
+        rounds = -(-units // sms)
+        assert 3 <= rounds <= 6, (sms, s)
+        assert units / (rounds * sms) >= 0.9, (sms, s)     # the last round is (nearly) full
+    assert pka.paged_attn_split_heuristic(p, 64, 8, num_sms=152) == 19    # 608 units = 4 x 152
+
+
 def test_plan_stage_writes_the_device_image(built_lib):
     """pa_plan_stage: the image goes to a host buffer, the device buffer is only bound."""
     import torch
