@@ -147,9 +147,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t *trow;
     };
     // Keys of a row of the unit's split: its visible range [lo, hi) (causal
-    // end, sliding window) cut by the split partition.  Both ends grow with
-    // the row's position, so the tile's key range runs from the first row's
-    // lower end to the last row's upper end: key tiles kt0 .. kt0 + n_kt - 1.
+    // end, sliding window) cut by the split partition.  Without a window (or
+    // split) both ends grow with the row's position, so the tile's key range
+    // runs from the first row's lower end to the last row's upper end: key
+    // tiles kt0 .. kt0 + n_kt - 1.
     auto row_keys = [&](const Unit &u, int pos, int64_t &j0, int64_t &j1) {
         int64_t lo, hi;
         visible_range(pos, u.seq_len, prm.causal, prm.window, lo, hi);
@@ -172,6 +173,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t first_j0, first_j1, last_j0, last_j1;
         row_keys(u, u.pos0, first_j0, first_j1);
         row_keys(u, u.pos0 + u.nq - 1, last_j0, last_j1);
+        if (prm.window > 0 && prm.splits > 1) {
+            // With a window the split base (lo rounded down to a page) moves
+            // along the tile, and a shorter page-rounded chunk after a move can
+            // start split s > 1 earlier than it did for the rows before.  Rows
+            // sharing a base form runs in which both ends only grow, so the
+            // extremes lie at the runs' first and last rows.
+            first_j0 = INT64_MAX;
+            last_j1 = 0;
+            for (int r = 0; r < u.nq;) {
+                int64_t lo, hi;
+                visible_range(u.pos0 + r, u.seq_len, prm.causal, prm.window, lo, hi);
+                // first row whose lower end reaches the next page
+                const int64_t next = (lo / ps + 1) * ps + prm.window - 1 - u.pos0;
+                const int r_end = (int)(next < u.nq ? next : u.nq) - 1;
+                int64_t a0, a1, b0, b1;
+                row_keys(u, u.pos0 + r, a0, a1);
+                row_keys(u, u.pos0 + r_end, b0, b1);
+                first_j0 = a0 < first_j0 ? a0 : first_j0;
+                last_j1 = b1 > last_j1 ? b1 : last_j1;
+                r = r_end + 1;
+            }
+            if (first_j0 > last_j1) first_j0 = last_j1;
+        }
         u.kt0 = (int)(first_j0 / kN);
         u.n_kt = last_j1 > first_j0 ? (int)((last_j1 + kN - 1) / kN) - u.kt0 : 0;
         return u;

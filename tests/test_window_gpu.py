@@ -176,3 +176,27 @@ def test_prefill_window_repeatable(cuda_device):
             first = out.clone()
         else:
             assert torch.equal(out.view(torch.int16), first.view(torch.int16))
+
+
+def test_mla_fp16_split_window(cuda_device):
+    """MLA in fp16 through the split path, with and without a window."""
+    seq_lens = [70, 500, 1300]
+    case = build_case("win_mla16", 58, seq_lens, decode_queries(seq_lens) + [(2, 640)], 128, 1, 512, 64, 64,
+                      torch.float16, 1 / math.sqrt(192), mla_p=64)
+    for w in (0, 300):
+        _compare(case, w, splits=3, what="mla fp16")
+
+
+def test_prefill_window_split_tile_range(cuda_device):
+    # With a window the page-rounded split chunk can shrink as a tile's rows
+    # move their base to the next page, so split s > 1 of a later row may start
+    # before that of an earlier row: the tile's key range has to cover every row,
+    # not only the first and the last.  Windows and split counts chosen so some
+    # tiles of this layout have such rows, causal and not.
+    seq_lens = [300, 900]
+    queries = [(0, i) for i in range(300)] + [(1, 500 + i) for i in range(200)]
+    case = build_case("win_pf_nc", 59, seq_lens, queries, 16, 4, 128, 128, 16, torch.bfloat16, 1 / math.sqrt(128))
+    for w in (0, 77, 400):
+        _compare(case, w, causal=False, splits=3, what="prefill non-causal split")
+    _compare(case, 82, splits=3, what="prefill causal split")
+    _compare(case, 50, splits=4, what="prefill causal split")
