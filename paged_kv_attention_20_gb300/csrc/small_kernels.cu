@@ -143,7 +143,11 @@ __global__ void __launch_bounds__(256) merge_kernel(AttnArgs a, int use_list, in
     for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
     const float inv = 1.f / tot;
     T *out = static_cast<T *>(a.out) + row * a.dv;
-    for (int c = lane * VEC; c < a.dv; c += 32 * VEC) {
+    // every lane runs every chunk (the weights are shuffled in the loop); a lane
+    // past the last column reads column 0 and stores nothing
+    for (int c0 = 0; c0 < a.dv; c0 += 32 * VEC) {
+        const bool live = c0 + lane * VEC < a.dv;
+        const int c = live ? c0 + lane * VEC : 0;
         float acc[VEC];
 #pragma unroll
         for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(256) merge_kernel(AttnArgs a, int use_list, in
         }
 #pragma unroll
         for (int i = 0; i < VEC; ++i) acc[i] *= inv;
-        OutVec<T, VEC>::store(out + c, acc);
+        if (live) OutVec<T, VEC>::store(out + c, acc);
     }
 }
 
