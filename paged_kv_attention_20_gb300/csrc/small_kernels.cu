@@ -167,9 +167,76 @@ __global__ void __launch_bounds__(256) merge_kernel(AttnArgs a, int use_list, in
     }
 }
 
+// Few rows or many splits: one 8-warp block per (query, head) row, warp w
+// taking splits w, w + 8, ...; the eight partial sums meet in shared memory.
+// Rows spread over every SM and all splits of a row are in flight at once,
+// where one warp per row would walk its splits one after another.
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256) merge_wide_kernel(AttnArgs a, int use_list) {
+    griddep_wait();
+    griddep_launch();
+    extern __shared__ float part[];   // [8][dv]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int item = blockIdx.x / a.hq, h = blockIdx.x - item * a.hq;
+    const int qi = use_list ? a.plan.decode[item] : item;
+    const int S = a.splits;
+    const int64_t rows = (int64_t)a.plan.queries * a.hq;
+    const int64_t row = (int64_t)qi * a.hq + h;
+    float m = -INFINITY;
+    for (int s = lane; s < S; s += 32) m = fmaxf(m, a.ws_lse[s * rows + row]);
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float wl[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int s = lane + 32 * k;
+        const float l = s < S ? a.ws_lse[s * rows + row] : -INFINITY;
+        wl[k] = l == -INFINITY ? 0.f : __expf(l - m);
+    }
+    float tot = wl[0] + wl[1];
+    for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    for (int c0 = 0; c0 < a.dv; c0 += 32 * VEC) {
+        const bool live = c0 + lane * VEC < a.dv;
+        const int c = live ? c0 + lane * VEC : 0;
+        float acc[VEC];
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
+#pragma unroll 4
+        for (int s = warp; s < S; s += 8) {
+            const float ws = __shfl_sync(0xffffffffu, s < 32 ? wl[0] : wl[1], s & 31);
+            float v[VEC];
+            load_vec<VEC>(a.ws_o + (s * rows + row) * a.dv + c, v);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) acc[i] += ws * v[i];
+        }
+        if (live) {
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) part[warp * a.dv + c + i] = acc[i];
+        }
+    }
+    __syncthreads();
+    const float inv = 1.f / tot;
+    T *out = static_cast<T *>(a.out) + row * a.dv;
+    for (int c = threadIdx.x; c < a.dv; c += 256) {
+        float x = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) x += part[w * a.dv + c];
+        out[c] = from_float<T>(x * inv);
+    }
+}
+
 template <int VEC> cudaError_t launch_merge_vec(const AttnArgs &a, bool use_list, int nrows, cudaStream_t st) {
-    const dim3 grid((unsigned)((nrows + 7) / 8)), block(256);
     const int ul = use_list ? 1 : 0;
+    if (nrows < 1024 || a.splits >= 16) {
+        // fewer rows than fill the GPU at 8 per block, or long split chains
+        const dim3 grid((unsigned)nrows), block(256);
+        const size_t smem = (size_t)8 * a.dv * sizeof(float);
+        switch (a.dtype) {
+            case PA_F32: return launch_pdl(merge_wide_kernel<float, VEC>, grid, block, smem, st, a, ul);
+            case PA_F16: return launch_pdl(merge_wide_kernel<__half, VEC>, grid, block, smem, st, a, ul);
+            default: return launch_pdl(merge_wide_kernel<__nv_bfloat16, VEC>, grid, block, smem, st, a, ul);
+        }
+    }
+    const dim3 grid((unsigned)((nrows + 7) / 8)), block(256);
     switch (a.dtype) {
         case PA_F32: return launch_pdl(merge_kernel<float, VEC>, grid, block, 0, st, a, ul, nrows);
         case PA_F16: return launch_pdl(merge_kernel<__half, VEC>, grid, block, 0, st, a, ul, nrows);

@@ -75,3 +75,16 @@ def test_large_pages_prefill(cuda_device, ps):
                       1 / math.sqrt(128))
     for splits in (None, 3):
         _compare(case, splits, what=f"prefill ps={ps}")
+
+
+@pytest.mark.parametrize("dv,dtype,splits", [(64, torch.bfloat16, 3), (3, torch.bfloat16, 3), (5, torch.float32, 2),
+                                             (64, torch.float16, 16)])
+def test_merge_paths(cuda_device, dv, dtype, splits):
+    # 64 queries x 16 heads = 1024 rows: below 16 splits the merge takes one warp
+    # per row (value dims under one warp's column chunk leave lanes idle), at 16
+    # or more one block per row; the small cases above cover the block path too
+    rng = np.random.default_rng(76)
+    seq_lens = [int(x) for x in rng.integers(1, 300, size=64)]
+    case = build_case("merge_paths", 76, seq_lens, decode_queries(seq_lens), 16, 4, 32, dv, 16, dtype,
+                      1 / math.sqrt(32))
+    _compare(case, splits, what=f"merge dv={dv} {dtype}")
