@@ -3,10 +3,11 @@
 ruDNN 0.1.7, src/paged_attention/mod.rs (`DevicePlan::attention`,
 `attention_into_split`): the same paged decode as every other path; here the
 query group of one KV head sits in the first rows of a 128-row tensor-core
-tile.  Groups 8..128, page sizes 8..256, ragged histories (1 key, one short of
-and one past a 128-key tile), splits whose first tile starts mid-tile, sliding
-windows, non-causal queries and fp16 are compared element by element, and the
-per-split partials and LSE with the oracle's partition.
+tile.  Groups 8..128 (powers of two and 12, 24, 40, 96), page sizes 8..256,
+ragged histories (1 key, one short of and one past a 128-key tile), splits
+whose first tile starts mid-tile, sliding windows, non-causal queries and fp16
+are compared element by element, and the per-split partials and LSE with the
+oracle's partition.
 """
 import math
 
@@ -30,7 +31,7 @@ def _compare(case, splits=None, causal=None, window=0, what=""):
     return assert_close(out.double().numpy(), ref, case.dtype, f"{what} splits={splits} window={window}")
 
 
-@pytest.mark.parametrize("hq,hkv", [(8, 1), (64, 8), (32, 2), (64, 1), (128, 1)])
+@pytest.mark.parametrize("hq,hkv", [(8, 1), (64, 8), (32, 2), (64, 1), (128, 1), (24, 2), (48, 2), (40, 1), (96, 1)])
 def test_groups(cuda_device, hq, hkv):
     case = build_case("tc_groups", 81, LENS, decode_queries(LENS), hq, hkv, 128, 128, 16, torch.bfloat16,
                       1 / math.sqrt(128))
