@@ -15,7 +15,6 @@ other query a decode item (largest position first, ties in packing order).
 import ctypes
 
 import numpy as np
-import pytest
 
 import paged_kv_attention_20_gb300 as pka
 from paged_kv_attention_20_gb300._binding import PagedAttentionError

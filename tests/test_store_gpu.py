@@ -4,7 +4,6 @@ ruDNN 0.1.7, src/paged_attention/mod.rs, `append_with_report`: new rows
 [queries, heads, d|dv] land at the plan's positions; a zero-size append does
 nothing.
 """
-import numpy as np
 import pytest
 import torch
 
