@@ -483,9 +483,17 @@ def cpu_baseline(case, budget_s=15.0):
     rows = np.linspace(0, nrows - 1, want).astype(np.int64)
     rows = np.unique(rows)
     t, b = oracle_rows_rate(case, rows)
+    passes = 1
+    # on many cores the whole workload can take well under the budget: repeat
+    # it, so the figure covers about ten seconds of work
+    while len(rows) == nrows and t < 0.66 * budget_s and passes < 1000:
+        dt, db = oracle_rows_rate(case, rows)
+        t, b, passes = t + dt, b + db, passes + 1
+    what = (f"{passes} passes over all {nrows} (query, head) rows of the GQA decode workload"
+            if len(rows) == nrows else
+            f"{len(rows)} of {nrows} (query, head) rows of the GQA decode workload, evenly spaced")
     return {"value": b / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{len(rows)} of {nrows} (query, head) rows of the GQA decode workload, evenly spaced; "
-                      f"{t:.1f} s on {threads} threads"}
+            "sample": f"{what}; {t:.1f} s on {threads} threads"}
 
 
 def reference_arm(args, rank, world):
