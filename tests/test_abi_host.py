@@ -243,3 +243,26 @@ def test_plan_advance_refusals(built_lib):
     d = plan([5], [[0]], [0], [4], 16, 1)
     assert lib.pa_plan_advance(d.handle, None) == 10
     assert lib.pa_plan_advance(None, None) == 1
+
+
+def test_status_names_and_per_thread_messages(built_lib):
+    """pa_status_string names every status the header declares; a failed call's
+    message stays with the thread that made it."""
+    import threading
+    lib = _lib()
+    text = open(HEADER).read()
+    enum = re.search(r"typedef enum \{(.*?)\} pa_status;", text, flags=re.S).group(1)
+    codes = {name: int(v) for name, v in re.findall(r"(PA_[A-Z_]+)\s*=\s*(\d+)", enum)}
+    assert codes["PA_OK"] == 0 and len(codes) == 11
+    for name, v in codes.items():
+        assert lib.pa_status_string(v).decode() == name
+    assert lib.pa_status_string(99).decode() == "PA_UNKNOWN"
+    with pytest.raises(PagedAttentionError) as ei:
+        plan([5], [[0]], [0], [9], 16, 1)                      # position past the sequence
+    assert ei.value.status == codes["PA_ERR_RANGE"]
+    assert "position" in lib.pa_last_error().decode()
+    seen = {}
+    t = threading.Thread(target=lambda: seen.setdefault("msg", lib.pa_last_error().decode()))
+    t.start()
+    t.join()
+    assert seen["msg"] == ""                                     # nothing failed on that thread
