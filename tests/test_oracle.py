@@ -399,3 +399,30 @@ def test_planted_mistakes_are_caught(plant):
         except AssertionError:
             failures += 1
     assert failures >= 1, f"planted mistake {plant} slipped through every pin"
+
+
+def test_rows_and_thread_counts_give_the_same_bits():
+    """The sampled parity tests ask the oracle for chosen (query, head) rows on
+    many threads: those must be exactly the rows of the full single-threaded
+    result, for plain, windowed and split attention and for MLA."""
+    import workloads
+    rng = np.random.default_rng(11)
+    c = workloads.gqa_decode_bf16(num_seqs=5, ctx_lo=30, ctx_hi=400)
+    args = (c.q, c.k_cache, c.v_cache, c.seq_lens, c.block_table, c.query_seq, c.query_pos, c.scale)
+    nrows = c.num_queries * c.hq
+    rows = np.sort(rng.choice(nrows, 37, replace=False))
+    for window in (0, 50):
+        full, lse = oracle.attention(*args, window=window, nthreads=1)
+        many, lse_many = oracle.attention(*args, window=window, nthreads=8)
+        assert np.array_equal(full, many) and np.array_equal(lse, lse_many)
+        sub, lse_sub = oracle.attention(*args, window=window, rows=rows, nthreads=3)
+        assert np.array_equal(sub, full.reshape(nrows, -1)[rows]) and np.array_equal(lse_sub, lse.reshape(-1)[rows])
+        part, lpart = oracle.attention_split(*args, splits=5, window=window, nthreads=1)
+        psub, lpsub = oracle.attention_split(*args, splits=5, window=window, rows=rows, nthreads=4)
+        assert np.array_equal(psub, part[:, rows]) and np.array_equal(lpsub, lpart[:, rows])
+    m = workloads.mla_decode_bf16(num_seqs=3, heads=8, ctx_lo=10, ctx_hi=300)
+    margs = (m.q, m.k_cache, m.k_cache, m.seq_lens, m.block_table, m.query_seq, m.query_pos, m.scale)
+    mfull, _ = oracle.attention(*margs, qp=m.qp, kp_cache=m.v_cache, nthreads=1)
+    mrows = np.array([0, 5, 9, 23])
+    msub, _ = oracle.attention(*margs, qp=m.qp, kp_cache=m.v_cache, rows=mrows, nthreads=6)
+    assert np.array_equal(msub, mfull.reshape(m.num_queries * m.hq, -1)[mrows])
