@@ -72,3 +72,17 @@ def test_refusals_with_an_uploaded_plan(cuda_device):
     with pytest.raises(ValueError, match="one shared head"):           # MLA caches with two heads
         pka.paged_mla_forward(plan, q, q[:, :, :8].contiguous(), k, k[..., :8].contiguous(), 0.1)
     assert pka.device_status() == 0
+
+
+def test_readme_calls_exist():
+    """Every package function the README's usage snippet calls is exported."""
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "README.md")).read()
+    snippet = re.search(r"```python\n(.*?)```", text, flags=re.S).group(1)
+    names = set(re.findall(r"\bpka\.(\w+)\(", snippet))
+    assert {"paged_attn_plan", "paged_kv_store", "paged_attn_forward", "paged_mla_forward"} <= names
+    for n in names:
+        assert callable(getattr(pka, n, None)), f"README calls pka.{n}, which the package does not export"
+    assert callable(getattr(pka.Plan, "stage", None))
