@@ -10,7 +10,8 @@ word image (staged to host memory) with what those rules and the documented
 work lists give: per query (seq, pos, slot = table[seq][pos / ps] * ps +
 pos % ps), runs of at least 16 consecutive positions of one sequence cut into
 prefill tiles of at most 128 queries (heaviest last position first), every
-other query a decode item (largest position first, ties in packing order).
+other query a decode item (largest position first, ties in packing order),
+and every query once more in that order.
 """
 import ctypes
 
@@ -141,6 +142,10 @@ def test_random_schedules_follow_the_rules(built_lib):
         got_tiles = [tuple(int(x) for x in w[o_til + 4 * t:o_til + 4 * t + 4]) for t in range(plan.n_tiles)]
         assert got_tiles == tiles
         assert plan.n_tile_queries == sum(t[2] for t in tiles)
+        # the last section: every query, largest position first (ties in packing order)
+        o_ord = o_til + 4 * plan.n_tiles
+        assert list(w[o_ord:o_ord + nq]) == sorted(range(nq), key=lambda q: -qpos[q])
+        assert int(w[13]) == -(-(o_ord + nq) // 4) * 4 and int(w[0]) == 0x50414731
         tiles_seen += len(tiles)
     # the draw reaches every outcome and builds prefill tiles, so the checks above bite
     assert min(seen.values()) > 100 and tiles_seen > 100, (seen, tiles_seen)
