@@ -6,7 +6,10 @@ new K/V rows into the paged cache (paged_kv_store) and run paged attention over
 every query (paged_attn_forward_split with the library's split heuristic, which
 launches the split-KV decode kernel and, when splits > 1, the LSE merge).  The
 schedule is built and uploaded once before timing (it is reused while the
-schedule is unchanged); the end-to-end leg re-uploads it every step.
+schedule is unchanged).  The end-to-end leg replays one CUDA graph per step:
+pinned host-to-device copies of the step's inputs, pa_plan_advance (the
+schedule moves one position on, on the device), the append, the attention and
+the device-to-host copy of the output.
 
 Main line: the Llama-3-8B-like GQA decode layer -- 64 sequences, one query each,
 Hq=32, Hkv=8, D=Dv=128, page_size=16, contexts U[512, 8192], bf16, shuffled
@@ -20,7 +23,8 @@ decode (TFLOP/s on causal-visible pairs), and MLA decode (TFLOP/s and KV GB/s).
 
 --impl reference times the fp64 CPU oracle on the host cores on bounded samples
 of the same workload (there is no other implementation to compare with).
-Multi-GPU: independent replicas (no exchange step exists), weak scaling.
+Multi-GPU: independent replicas (no exchange step exists), weak scaling; a
+multi-rank run times the decode workloads only (see secondary_for_run).
 """
 from __future__ import annotations
 
@@ -353,6 +357,21 @@ def e2e_leg(case, device, steps: int, warmup: int):
                     "on the device); paged_kv_store; paged_attn_forward_split; D2H of the output; host wait"}
 
 
+DECODE_ONLY = ("long", "gqa")
+
+
+def secondary_for_run(requested: str, world: int) -> list:
+    """Secondary workloads a run measures.  A multi-rank run (one replica per
+    GPU) keeps to the decode workloads, whose kernels read only their own
+    GPU's memory through plain per-CTA TMA loads: it launches no prefill and
+    no MLA kernel, so no thread-block-cluster kernel runs in a job that spans
+    several GPUs."""
+    which = [w for w in requested.split(",") if w]
+    if world > 1:
+        which = [w for w in which if w in DECODE_ONLY]
+    return which
+
+
 def secondary(device, warmup: int, steps: int, peaks, which):
     """Long-context split decode, mixed prefill + decode, MLA decode (one entry each)."""
     import workloads
@@ -639,7 +658,7 @@ def main():
     del step
     torch.cuda.empty_cache()
     line["e2e"] = e2e_leg(case, device, steps=max(10, min(args.steps, 200)), warmup=args.warmup)
-    which = [w for w in args.secondary.split(",") if w]
+    which = secondary_for_run(args.secondary, world)
     if which:
         line["workloads"] = secondary(device, args.warmup, 20, peaks, which)
     if not args.no_cpu_baseline:

@@ -25,6 +25,10 @@
  *    propagates into that query's output and is not checked (module doc).
  *    Cache slots no query can see (pages no sequence references, slots past a
  *    sequence's length) are never read and may hold anything.
+ *  - Every device pointer must be device memory of the current device
+ *    (cudaMalloc or a pool allocator on it): host memory, pinned or mapped,
+ *    managed memory and peer GPUs' memory are refused with PA_ERR_ARG before
+ *    anything is launched (`check_tensor`: every operand on Q's device).
  *  - `out` must not overlap any input (`attention_into`, safety contract).
  *  - Element types: PA_F32, PA_F16, PA_BF16 for every floating operand of a
  *    call (one dtype per call, `check_tensor`); accumulation is fp32 and the
@@ -298,11 +302,15 @@ pa_status paged_mla_forward(const pa_plan *plan, const void *q, const void *qp,
  * array of PA_STATIC_SCRATCH_BYTES that every GPU loading the library holds
  * until the process exits.  The caller still owns q, the caches and out.
  *
- * Rejects (PA_ERR_WORKSPACE) any plan/heads/value_dim/splits whose
- * pa_workspace_bytes exceeds PA_STATIC_SCRATCH_BYTES.  Calls no cudaMalloc,
- * cudaFree or allocating library routine.  The first call on a device looks up
- * the array's device address with that device current; make it before any
- * stream capture.  All calls share the array and it keeps the last call's
+ * The argument checks of paged_attn_forward_split run first and return the
+ * same statuses; then any plan/heads/value_dim/splits whose
+ * pa_workspace_bytes exceeds PA_STATIC_SCRATCH_BYTES is rejected
+ * (PA_ERR_WORKSPACE).  Calls no cudaMalloc, cudaFree or allocating library
+ * routine.  The first call on a device looks up the array's device address
+ * with that device current and keeps it; make that call before any stream
+ * capture, and do not call this entry point on a device after a
+ * cudaDeviceReset of it (the reset may move the array).  All calls share the
+ * array and it keeps the last call's
  * contents (each call writes every entry it later reads, so nothing needs
  * clearing); calls whose GPU work overlaps race on it -- serialise them on one
  * stream.
@@ -329,7 +337,9 @@ pa_status pa_time_next_kernel(void *start_event, void *stop_event);
  * memory) bound every wait; a wait that runs out sets this word to a non-zero
  * code (PA_DEVICE_TIMEOUT_*) and the kernel returns early, leaving the context
  * usable.  This call synchronises the current device, reads the word and
- * optionally clears it; it is a diagnostic, not part of the hot path.
+ * optionally clears it; it is a diagnostic, not part of the hot path.  The
+ * word's device address is looked up once per device and kept, so a process
+ * that calls cudaDeviceReset must not use the library on that device again.
  */
 #define PA_DEVICE_TIMEOUT_TMA 1
 #define PA_DEVICE_TIMEOUT_MMA 2

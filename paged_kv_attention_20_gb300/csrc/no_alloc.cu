@@ -12,7 +12,10 @@
 // The array's host-side name is only a stand-in: host code must not pass it
 // to a kernel.  Its device address is looked up once per device with
 // cudaGetSymbolAddress (with that device current) on the first call made on
-// that device; make that first call before any stream capture.
+// that device; make that first call before any stream capture.  A
+// cudaDeviceReset unloads the module and may move the array, so the address
+// kept from before a reset must not be used after it: a process that resets a
+// device does not call this entry point on that device again.
 //
 // Every call shares the array and it keeps the previous call's contents.  The
 // split kernels write every partial and log-sum-exp entry that the merge of
@@ -55,8 +58,14 @@ extern "C" pa_status paged_attn_forward_split_static(const pa_plan *plan, const 
                                                      int32_t num_kv_heads, int32_t head_dim, int32_t value_dim,
                                                      float scale, int32_t causal, int32_t window, pa_dtype dtype,
                                                      int32_t splits, pa_stream_t stream) {
+    // the same argument checks, in the same order, as the workspace form, so an
+    // invalid call gets the status that form would give before any size check
+    static const char kName[] = "paged_attn_forward_split_static";
+    pa_status st = pa::check_attention_args(plan, num_heads, num_kv_heads, head_dim, value_dim, 0, scale, causal,
+                                            window, dtype, false, kName);
+    if (st != PA_OK) return st;
     int64_t counts[8];
-    pa_status st = pa_plan_describe(plan, counts);
+    st = pa_plan_describe(plan, counts);
     if (st != PA_OK) return st;
     if (splits < 1 || splits > PA_MAX_SPLITS)
         return pa_fail_with(PA_ERR_SPLITS, "paged_attn_forward_split_static: splits must be in 1..64");

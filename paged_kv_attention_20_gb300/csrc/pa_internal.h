@@ -89,6 +89,14 @@ __host__ __device__ inline void split_bounds(int64_t lo, int64_t hi, int splits,
     j1 = e;
 }
 
+// The attention entry points' argument checks that need no device: plan,
+// dtype, head counts and dims, scale, causal flag, window, MLA position dim
+// and the size bounds.  PA_OK or the status (and message) the entry point
+// named `name` returns for the first failing check.
+pa_status check_attention_args(const pa_plan *plan, int32_t hq, int32_t hkv, int32_t d, int32_t dv, int32_t p,
+                               float scale, int32_t causal, int32_t window, pa_dtype dtype, bool mla,
+                               const char *name);
+
 // Launchers (return cudaGetLastError() of the launch).
 // use_decode_list: iterate over plan.decode (else over every query).
 cudaError_t launch_kv_store(const PlanView &plan, const void *new_k, const void *new_v, void *k_cache,

@@ -68,6 +68,37 @@ pa::PlanView view_of(const pa_plan *p) {
 
 bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// True when `ptr` is device memory of the current device.  The kernels'
+// tensor maps and loads address only this GPU's own memory, so host memory
+// (pinned or not), managed memory and other GPUs' memory are refused.
+bool on_current_device(const void *ptr, int dev) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
+// PA_OK when every non-null pointer of `ptrs` is device memory of the current
+// device, else PA_ERR_ARG naming the operand.
+pa_status operands_on_device(const void *const *ptrs, const char *const *names, int n, const char *call) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PA_ERR_CUDA, "no current CUDA device");
+    }
+    for (int i = 0; i < n; ++i) {
+        if (ptrs[i] && !on_current_device(ptrs[i], dev)) {
+            char msg[256];
+            std::snprintf(msg, sizeof msg, "%s: %s is not device memory of the current device", call, names[i]);
+            return fail(PA_ERR_ARG, msg);
+        }
+    }
+    return PA_OK;
+}
+
+
 }  // namespace
 
 pa_status pa_fail_with(pa_status status, const char *msg) { return fail(status, msg); }
@@ -359,6 +390,12 @@ pa_status paged_kv_store(const pa_plan *plan, const void *new_k, const void *new
     if (plan->queries == 0) return PA_OK;  // no-op append
     if (!plan->dev) return fail(PA_ERR_STATE, "paged_kv_store: plan not uploaded");
     if (!new_k || !new_v || !k_cache || !v_cache) return fail(PA_ERR_ARG, "paged_kv_store: null tensor");
+    {
+        const void *ptrs[] = {new_k, new_v, k_cache, v_cache};
+        const char *names[] = {"new_k", "new_v", "k_cache", "v_cache"};
+        pa_status on_dev = operands_on_device(ptrs, names, 4, "paged_kv_store");
+        if (on_dev != PA_OK) return on_dev;
+    }
     cudaError_t e = pa::launch_kv_store(view_of(plan), new_k, new_v, k_cache, v_cache, num_heads, head_dim,
                                         value_dim, elem_bytes(dtype), (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e, "paged_kv_store launch");
@@ -367,13 +404,12 @@ pa_status paged_kv_store(const pa_plan *plan, const void *new_k, const void *new
 
 }  // extern "C"
 
-namespace {
-
-// Shared body of the attention entry points.
-pa_status attention(const pa_plan *plan, const void *q, const void *k, const void *v, const void *qp,
-                    const void *kp, void *out, int32_t hq, int32_t hkv, int32_t d, int32_t dv, int32_t p,
-                    float scale, int32_t causal, int32_t window, pa_dtype dtype, void *ws, size_t ws_bytes, int32_t splits,
-                    bool split_call, bool mla, cudaStream_t st, const char *name) {
+// The argument checks of the attention entry points that need no device
+// (`execute_attention_into`, `check_tensor`, `bounded`), in the order the
+// calls apply them.
+pa_status pa::check_attention_args(const pa_plan *plan, int32_t hq, int32_t hkv, int32_t d, int32_t dv, int32_t p,
+                                   float scale, int32_t causal, int32_t window, pa_dtype dtype, bool mla,
+                                   const char *name) {
     char msg[256];
     auto bad = [&](pa_status s, const char *what) {
         std::snprintf(msg, sizeof msg, "%s: %s", name, what);
@@ -393,6 +429,23 @@ pa_status attention(const pa_plan *plan, const void *q, const void *k, const voi
     if (hq > 65535) return bad(PA_ERR_LIMIT, "num_heads above the launch grid limit");
     if ((int64_t)plan->queries * hq * std::max(d, dv) > ((int64_t)1 << 40))
         return bad(PA_ERR_RANGE, "tensor too large");
+    return PA_OK;
+}
+
+namespace {
+
+// Shared body of the attention entry points.
+pa_status attention(const pa_plan *plan, const void *q, const void *k, const void *v, const void *qp,
+                    const void *kp, void *out, int32_t hq, int32_t hkv, int32_t d, int32_t dv, int32_t p,
+                    float scale, int32_t causal, int32_t window, pa_dtype dtype, void *ws, size_t ws_bytes, int32_t splits,
+                    bool split_call, bool mla, cudaStream_t st, const char *name) {
+    char msg[256];
+    auto bad = [&](pa_status s, const char *what) {
+        std::snprintf(msg, sizeof msg, "%s: %s", name, what);
+        return fail(s, msg);
+    };
+    pa_status checked = pa::check_attention_args(plan, hq, hkv, d, dv, p, scale, causal, window, dtype, mla, name);
+    if (checked != PA_OK) return checked;
     if (split_call) {
         if (splits < 1 || splits > PA_MAX_SPLITS) return bad(PA_ERR_SPLITS, "splits must be in 1..64");
         if (splits > 1 || ws) {
@@ -408,6 +461,13 @@ pa_status attention(const pa_plan *plan, const void *q, const void *k, const voi
     if (plan->queries == 0) return PA_OK;  // nothing to launch
     if (!plan->dev) return bad(PA_ERR_STATE, "plan not uploaded");
     if (!q || !k || !v || !out || (mla && (!qp || !kp))) return bad(PA_ERR_ARG, "null tensor");
+    {
+        const void *ptrs[] = {q, k, v, out, qp, kp, splits > 1 ? ws : nullptr};
+        const char *names[] = {"q", "the key cache", "the value cache", "out", "the position query",
+                               "the position cache", "the workspace"};
+        pa_status on_dev = operands_on_device(ptrs, names, 7, name);
+        if (on_dev != PA_OK) return on_dev;
+    }
 
     pa::AttnArgs a{};
     a.plan = view_of(plan);
