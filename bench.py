@@ -292,30 +292,32 @@ def soak_clocks(step: DecodeStep, device, seconds=1.0):
 def e2e_leg(case, device, steps: int, warmup: int):
     """Same metric through the public API with host buffers, run as a decode
     loop replays its attention layer: one CUDA graph holds the pinned host-to-
-    device copy of the step's inputs (q, new_k, new_v), pa_plan_advance (every
-    query moves one position on, on the device), the append, the split
-    attention and the device-to-host copy of the output; per step the host
-    replays it and waits.  The case is the GQA decode workload with its pages
-    reserved for the positions the loop reaches; the KV bytes are counted per
-    step as the histories grow.  The last replay is checked against the same
-    attention called directly."""
+    device copy of the step's inputs (q, the position query for MLA, and the new
+    cache rows), pa_plan_advance (every query moves one position on, on the
+    device), the append, the attention (split GQA, or MLA) and the device-to-host
+    copy of the output; per step the host replays it and waits.  The case is the
+    given decode workload with its pages reserved for the positions the loop
+    reaches; the KV bytes (and, for MLA, the flops) are counted per step as the
+    histories grow.  The last replay is checked against the same attention
+    called directly."""
     import workloads
     import paged_kv_attention_20_gb300 as pka
     total = warmup + steps + 2
     ctx = [int(n) for n in case.seq_lens]
     grown = workloads.build_case(case.name + "_loop", case.meta["seed"], [n + total for n in ctx],
-                                 [(i, n - 1) for i, n in enumerate(ctx)], case.hq, case.hkv, case.d, case.dv,
-                                 case.page_size, case.dtype, case.scale)
+                                 [(i, n - 1) for i, n in enumerate(ctx)], case.hq, case.hkv, case.d,
+                                 case.p if case.is_mla else case.dv, case.page_size, case.dtype, case.scale,
+                                 mla_p=case.p)
     step = DecodeStep(grown, device)
-    host = {k: getattr(grown, k).pin_memory() for k in ("q", "new_k", "new_v")}
+    names = ("q", "qp", "new_k", "new_v") if grown.is_mla else ("q", "new_k", "new_v")
+    host = {k: getattr(grown, k).pin_memory() for k in names}
     out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * out_host.element_size()
 
     def body():
-        step.dc.q.copy_(host["q"], non_blocking=True)
-        step.dc.new_k.copy_(host["new_k"], non_blocking=True)
-        step.dc.new_v.copy_(host["new_v"], non_blocking=True)
+        for k in names:
+            getattr(step.dc, k).copy_(host[k], non_blocking=True)
         pka.paged_attn_plan_advance(step.plan)
         step.store()
         step.attend()
@@ -344,17 +346,27 @@ def e2e_leg(case, device, steps: int, warmup: int):
         one()
     dt = time.perf_counter() - t
     # positions during timed step i: ctx - 1 + done + 1 + i; keys seen: that + 1
-    per_tok = grown.hkv * (grown.d + grown.dv) * grown.new_k.element_size()
-    kv = sum((sum(ctx) + len(ctx) * (done + 1 + i)) * per_tok for i in range(steps))
+    elt = grown.new_k.element_size()
+    if grown.is_mla:
+        per_tok = (grown.d + grown.p) * elt
+        per_key_flops = grown.hq * (2 * (grown.d + grown.p) + 2 * grown.d)
+    else:
+        per_tok = grown.hkv * (grown.d + grown.dv) * elt
+        per_key_flops = grown.hq * (2 * grown.d + 2 * grown.dv)
+    keys = sum(sum(ctx) + len(ctx) * (done + 1 + i) for i in range(steps))
     last = out_host.clone()
     step.attend()                    # the same attention on the state the last replay left
     torch.cuda.synchronize(device)
     if not torch.equal(step.out.cpu(), last) or pka.device_status() != 0:
         raise RuntimeError("graph-replayed decode step differs from the direct call")
-    return {"value": kv / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": dt / steps * 1e3,
-            "mode": "per step one CUDA graph replay: pinned H2D of q, new_k, new_v; pa_plan_advance (schedule "
-                    "on the device); paged_kv_store; paged_attn_forward_split; D2H of the output; host wait"}
+    what = "paged_mla_forward" if grown.is_mla else "paged_attn_forward_split"
+    res = {"value": keys * per_tok / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h), "ms_per_step": dt / steps * 1e3, "splits": step.splits,
+           "mode": f"per step one CUDA graph replay: pinned H2D of {', '.join(names)}; pa_plan_advance "
+                   f"(schedule on the device); paged_kv_store; {what}; D2H of the output; host wait"}
+    if grown.is_mla:
+        res.update(value=keys * per_key_flops / dt / 1e12, unit="TFLOP/s", kv_gbs=keys * per_tok / dt / 1e9)
+    return res
 
 
 DECODE_ONLY = ("long", "gqa")
@@ -372,13 +384,15 @@ def secondary_for_run(requested: str, world: int) -> list:
     return which
 
 
-def secondary(device, warmup: int, steps: int, peaks, which):
-    """Long-context split decode, mixed prefill + decode, MLA decode (one entry each)."""
+def secondary(device, warmup: int, steps: int, peaks, which, cpu=True):
+    """Long-context split decode, mixed prefill + decode, MLA decode (one entry each);
+    with cpu=True each entry also carries the oracle timed on the host cores over
+    the same inputs (cpu_baseline, in the entry's own unit)."""
     import workloads
     res = {}
     hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops"]
     if "long" in which:
-        res.update(_long_context(device, warmup, steps, hbm))
+        res.update(_long_context(device, warmup, steps, hbm, cpu))
     if "gqa" in which:
         res.update(_split_sweep(workloads.gqa_decode_bf16(), "gqa_decode_bf16_split_sweep",
                                 "64 seqs ctx U[512,8192], Hq=32, Hkv=8, D=128, ps=16, bf16",
@@ -414,6 +428,7 @@ def secondary(device, warmup: int, steps: int, peaks, which):
         if case.is_mla:
             res[name].update(kernel_ms=kms, kernel_tflops=fl / kms / 1e9, kernel_frac_bf16_peak=fl / kms / 1e9 / tc,
                              kv_gbs=kv_bytes(case) / ms / 1e6, frac_hbm=kv_bytes(case) / ms / 1e6 / hbm)
+            res[name]["e2e"] = e2e_leg(case, device, steps=max(10, steps), warmup=warmup)
         else:
             # prefill chunks are the first n_prefill * chunk queries; their kernel is timed alone
             # (the call then runs the decode items, an HBM-bound kernel, after it)
@@ -423,16 +438,23 @@ def secondary(device, warmup: int, steps: int, peaks, which):
                              prefill_kernel_frac_bf16_peak=pfl / kms / 1e9 / tc,
                              decode_kv_bytes=kv_bytes(case, npq), note="ms and tflops cover the whole call: the "
                              "prefill kernel, then the decode items (HBM-bound)")
+        if cpu:
+            label = "MLA decode workload" if case.is_mla else "mixed prefill + decode workload"
+            res[name]["cpu_baseline"] = cpu_baseline(case, label, unit="TFLOP/s")
         del st, case
         torch.cuda.empty_cache()
     return res
 
 
-def _long_context(device, warmup, steps, hbm):
+def _long_context(device, warmup, steps, hbm, cpu=False):
     import workloads
-    return _split_sweep(workloads.long_context_decode_bf16(), "long_context_split_decode_bf16",
-                        "4 seqs ctx {32K,64K,96K,128K}, Hq=64, Hkv=8, D=128, ps=16, bf16",
-                        (None, 1, 4, 8, 16, 32, 64), device, warmup, steps, hbm)
+    case = workloads.long_context_decode_bf16()
+    res = _split_sweep(case, "long_context_split_decode_bf16",
+                       "4 seqs ctx {32K,64K,96K,128K}, Hq=64, Hkv=8, D=128, ps=16, bf16",
+                       (None, 1, 4, 8, 16, 32, 64), device, warmup, steps, hbm)
+    if cpu:
+        res["long_context_split_decode_bf16"]["cpu_baseline"] = cpu_baseline(case, "long-context decode workload")
+    return res
 
 
 def _split_sweep(c3, name, desc, counts, device, warmup, steps, hbm):
@@ -480,38 +502,57 @@ def _split_sweep(c3, name, desc, counts, device, warmup, steps, hbm):
 
 def oracle_rows_rate(case, rows, nthreads=0):
     """Run the oracle on flat (q*Hq+h) rows; return (seconds, algorithmic KV bytes covered)."""
+    dt, b, _ = oracle_rows_work(case, rows, nthreads)
+    return dt, b
+
+
+def oracle_rows_work(case, rows, nthreads=0):
+    """Run the oracle on flat (q*Hq+h) rows; return (seconds, algorithmic KV bytes, flops) those
+    rows account for: each row's share of its query's KV bytes (kv_bytes) and its own flops
+    over its causal-visible keys (attn_flops)."""
     import oracle
     q_of = np.asarray(rows) // case.hq
-    vis = visible_counts(case)[q_of]
+    n = float(visible_counts(case)[q_of].sum())
     elt = torch.empty((), dtype=case.dtype).element_size()
-    per_row = case.hkv * (case.d + case.dv) * elt / case.hq       # each row's share of its query's bytes
     t = time.perf_counter()
-    oracle.attention(case.q, case.k_cache, case.v_cache, case.seq_lens, case.block_table, case.query_seq,
-                     case.query_pos, case.scale, rows=rows, nthreads=nthreads)
-    return time.perf_counter() - t, float(vis.sum() * per_row)
+    if case.is_mla:
+        oracle.attention(case.q, case.k_cache, case.k_cache, case.seq_lens, case.block_table, case.query_seq,
+                         case.query_pos, case.scale, qp=case.qp, kp_cache=case.v_cache, rows=rows,
+                         nthreads=nthreads)
+        per_key_bytes = (case.d + case.p) * elt / case.hq          # one shared latent head per query
+        per_key_flops = 2 * (case.d + case.p) + 2 * case.d
+    else:
+        oracle.attention(case.q, case.k_cache, case.v_cache, case.seq_lens, case.block_table, case.query_seq,
+                         case.query_pos, case.scale, rows=rows, nthreads=nthreads)
+        per_key_bytes = case.hkv * (case.d + case.dv) * elt / case.hq   # each KV head once per query
+        per_key_flops = 2 * case.d + 2 * case.dv
+    return time.perf_counter() - t, n * per_key_bytes, n * per_key_flops
 
 
-def cpu_baseline(case, budget_s=15.0):
+def cpu_baseline(case, label="GQA decode workload", unit="GB/s", budget_s=12.0):
+    """The oracle, as it stands, on all host cores over a bounded, evenly spaced
+    sample of the workload's (query, head) rows, reported in `unit` (GB/s of
+    algorithmic KV bytes, or TFLOP/s over causal-visible pairs; both figures are
+    given).  When the whole workload takes well under the budget it is repeated
+    so the figure covers about `budget_s` seconds of work."""
     import oracle
     threads = oracle.threads()
     nrows = case.num_queries * case.hq
-    probe = np.arange(min(nrows, max(threads, 32)))
-    t, b = oracle_rows_rate(case, probe)
-    rate = b / max(t, 1e-9)
+    probe = np.unique(np.linspace(0, nrows - 1, min(nrows, max(threads, 32))).astype(np.int64))
+    t, _, _ = oracle_rows_work(case, probe)
     want = int(min(nrows, max(len(probe), len(probe) * budget_s / max(t, 1e-6))))
-    rows = np.linspace(0, nrows - 1, want).astype(np.int64)
-    rows = np.unique(rows)
-    t, b = oracle_rows_rate(case, rows)
+    rows = np.unique(np.linspace(0, nrows - 1, want).astype(np.int64))
+    t, b, f = oracle_rows_work(case, rows)
     passes = 1
-    # on many cores the whole workload can take well under the budget: repeat
-    # it, so the figure covers about ten seconds of work
     while len(rows) == nrows and t < 0.66 * budget_s and passes < 1000:
-        dt, db = oracle_rows_rate(case, rows)
-        t, b, passes = t + dt, b + db, passes + 1
-    what = (f"{passes} passes over all {nrows} (query, head) rows of the GQA decode workload"
+        dt, db, df = oracle_rows_work(case, rows)
+        t, b, f, passes = t + dt, b + db, f + df, passes + 1
+    what = (f"{passes} passes over all {nrows} (query, head) rows of the {label}"
             if len(rows) == nrows else
-            f"{len(rows)} of {nrows} (query, head) rows of the GQA decode workload, evenly spaced")
-    return {"value": b / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            f"{len(rows)} of {nrows} (query, head) rows of the {label}, evenly spaced")
+    gbs, tflops = b / t / 1e9, f / t / 1e12
+    return {"value": gbs if unit == "GB/s" else tflops, "unit": unit, "cores": threads, "kind": "oracle",
+            "kv_gbs": gbs, "tflops": tflops, "seconds": t,
             "sample": f"{what}; {t:.1f} s on {threads} threads"}
 
 
@@ -660,9 +701,9 @@ def main():
     line["e2e"] = e2e_leg(case, device, steps=max(10, min(args.steps, 200)), warmup=args.warmup)
     which = secondary_for_run(args.secondary, world)
     if which:
-        line["workloads"] = secondary(device, args.warmup, 20, peaks, which)
+        line["workloads"] = secondary(device, args.warmup, 20, peaks, which, cpu=not args.no_cpu_baseline)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(case.to("cpu"))
+        line["cpu_baseline"] = cpu_baseline(case)
     print(json.dumps(line), flush=True)
     barrier(world)
 

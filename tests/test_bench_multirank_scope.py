@@ -46,7 +46,7 @@ def _run_main(monkeypatch, world, rank):
     monkeypatch.setattr(bench, "e2e_leg", lambda *a, **k: {"value": 1.0})
     monkeypatch.setattr(bench, "cpu_baseline", lambda *a, **k: {"value": 1.0})
     monkeypatch.setattr(bench, "profile_traffic", lambda *a, **k: None)
-    monkeypatch.setattr(bench, "secondary", lambda device, w, s, peaks, which: calls["secondary"].append(list(which)) or {})
+    monkeypatch.setattr(bench, "secondary", lambda device, w, s, peaks, which, **k: calls["secondary"].append(list(which)) or {})
     monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", str(world), "--steps", "2", "--warmup", "3",
                                       "--no-cpu-baseline"])
     bench.main()
