@@ -7,7 +7,7 @@
 // sees keys 0..p_i: the cached context plus the chunk's earlier rows.
 //
 // Work unit: (tile of up to 128 consecutive queries, split, query head).  The
-// kernel is persistent: as many clusters as fit on the GPU at once, walking
+// kernel is persistent: one CTA per SM, walking
 // the units (heaviest first) in serpentine rounds, so the K/V rings stream on from
 // one unit into the next, Q of the next unit loads while the last tiles of
 // the current one finish, and a CTA's start-up and teardown are paid once
@@ -18,15 +18,17 @@
 //   warps 8/10 TMA producers: Q of each unit and K tiles (warp 8), V tiles (warp 10)
 //              of 128 keys gathered page by page through the block table
 //              (one box per page and 64-column half, 128-byte swizzle), each
-//              through its own ring, so K is released once S is computed;
+//              through its own ring, so K is released once S is computed; the
+//              block-table load of a tile's pages is issued one tile ahead;
 //   warps 9/11 MMA issuers: warp 9 issues S = Q K^T into one of three TMEM
 //              buffers, warp 11 issues O += P V with P read from tensor memory
 //              (the softmax warps overwrite their row of the S buffer with P as
 //              16-bit pairs); two issuers, because the tensor core takes only a
 //              few MMAs ahead and one thread blocked on S noticed P late.
 // K and V tiles use 3-stage shared-memory rings; P never touches shared memory.
-// CTAs of a cluster (query heads of one KV head, same query tile) receive each
-// K/V tile by multicast: one L2 read feeds all of them.
+// Each CTA loads its own tiles, from this GPU's memory only (no thread-block
+// cluster, no multicast); the query heads of one KV head read the same tiles,
+// which L2 serves after the first of them.
 // Key tiles past the last query's position are never loaded; the diagonal
 // tiles are masked per row.  Keys at or past the sequence length never reach
 // P.V: their scores are masked and their V rows are zeroed in shared memory
@@ -68,9 +70,9 @@ struct Smem {
     uint64_t q_empty;              // every S MMA of the unit done: the Q buffer may be refilled
     uint64_t o_free;               // the softmax warps have read O of the unit (all 256 threads)
     uint64_t k_full[kStages];      // K tile landed
-    uint64_t k_empty[kStages];     // S of the tile done in every CTA of the cluster (K free)
+    uint64_t k_empty[kStages];     // S of the tile done (K free)
     uint64_t v_full[kStages];
-    uint64_t v_empty[kStages];     // P.V of the tile done in every CTA of the cluster (V free)
+    uint64_t v_empty[kStages];     // P.V of the tile done (V free)
     uint64_t s_full[3];            // S of tile kt in TMEM buffer kt % 3
     uint64_t p_ready[3];           // P of tile kt in TMEM (all 256 softmax threads) -> p_ready[kt % 3].
                                    // One barrier per tile in flight: S runs two tiles ahead, so warps
@@ -129,18 +131,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     Smem &s = *reinterpret_cast<Smem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // Persistent: each cluster walks its share of the U units, a unit
-    // being (query tile, split, csize consecutive query heads) in the order
-    // block = (tile * splits + split) * Hq + head; the plan orders tiles by
-    // decreasing key count, so the heaviest units go first.  Every role walks
-    // the same units; ring stages, S buffers and their barrier phases follow
-    // one tile counter that runs on across units, so the K/V rings stream
-    // without a break from one unit into the next.
-    const uint32_t crank = cluster_ctarank(), csize = cluster_nctarank();
-    const uint16_t cmask = (uint16_t)((1u << csize) - 1u);
-    const int cluster = (int)(blockIdx.x / csize);
-    const int n_clusters = (int)(gridDim.x / csize);
-    const int units = prm.plan.n_tiles * prm.splits * prm.hq / (int)csize;
+    // Persistent: each CTA walks its share of the units, a unit being (query
+    // tile, split, query head) in the order unit = (tile * splits + split) *
+    // Hq + head; the plan orders tiles by decreasing key count, so the
+    // heaviest units go first.  Every role walks the same units; ring stages,
+    // S buffers and their barrier phases follow one tile counter that runs on
+    // across units, so the K/V rings stream without a break from one unit into
+    // the next.
+    const int cta = (int)blockIdx.x;
+    const int n_ctas = (int)gridDim.x;
+    const int units = prm.plan.n_tiles * prm.splits * prm.hq;
     const int ps = prm.plan.page_size;
     struct Unit {
         int split, h, kvh, q0, nq, pos0, seq_len, kt0, n_kt;
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto unit_at = [&](int ui) -> Unit {
         Unit u;
-        const int b = ui * (int)csize + (int)crank;
+        const int b = ui;
         const int tile_idx = b / (prm.hq * prm.splits);
         u.split = (b / prm.hq) % prm.splits;
         u.h = b % prm.hq;
@@ -201,13 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         return u;
     };
 
-    // The cluster's i-th unit: round i of n_clusters-sized rounds, taken in
-    // serpentine order (odd rounds from the last cluster down), so with units
-    // sorted by decreasing size the clusters' totals even out.  A cluster whose
-    // slot in the last, partial round lies past the end has no i-th unit.
+    // The CTA's i-th unit: round i of n_ctas-sized rounds, taken in serpentine
+    // order (odd rounds from the last CTA down), so with units sorted by
+    // decreasing size the CTAs' totals even out.  A CTA whose slot in the
+    // last, partial round lies past the end has no i-th unit.
     auto unit_of = [&](int i) -> int {
-        const int slot = (i & 1) ? n_clusters - 1 - cluster : cluster;
-        const int ui = i * n_clusters + slot;
+        const int slot = (i & 1) ? n_ctas - 1 - cta : cta;
+        const int ui = i * n_ctas + slot;
         return ui < units ? ui : units;
     };
 
@@ -217,9 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&s.o_free, 2 * kM);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&s.k_full[i], 1);
-            mbar_init(&s.k_empty[i], csize);       // one release per CTA of the cluster
+            mbar_init(&s.k_empty[i], 1);
             mbar_init(&s.v_full[i], 1);
-            mbar_init(&s.v_empty[i], csize);
+            mbar_init(&s.v_empty[i], 1);
         }
         for (int i = 0; i < 3; ++i) mbar_init(&s.s_full[i], 1);
         for (int i = 0; i < 3; ++i) mbar_init(&s.p_ready[i], 2 * kM);
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    cluster_barrier();       // every barrier of the cluster exists before any multicast lands
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
     auto tmem_s = [tmem](int b) -> uint32_t { return tmem + 128u * (uint32_t)b; };   // S / P buffers 0..2
@@ -247,8 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // its own 3-stage ring: a K stage is free as soon as S of its tile is
         // computed, a V stage only after P.V, so K runs ahead of V.  Lane 0 owns
         // the barriers; lanes 0..pages_per_tile-1 each gather one page (two
-        // 64-column boxes).  In a cluster, box j of page p is issued by CTA
-        // (2p + j) % csize and multicast to all.  Q of the next unit is loaded
+        // 64-column boxes).  Q of the next unit is loaded
         // once every S MMA of the previous unit has completed.
         const bool is_k = warp == 8;
         const int pages_per_tile = kN / ps;
@@ -276,7 +275,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
             const int used_pages = (u.seq_len + ps - 1) / ps;
+            // this lane's page of key tile kt; the block-table load of the next
+            // tile is issued before the wait for a free stage, so its latency is
+            // off the refill's critical path
+            auto page_row = [&](int kt) -> int {
+                const int lp = (u.kt0 + kt) * pages_per_tile + lane;
+                return lp < used_pages ? u.trow[lp] * ps : oob_row;
+            };
+            int row_next = lane < pages_per_tile && u.n_kt > 0 ? page_row(0) : 0;
             for (int kt = 0; go && kt < u.n_kt; ++kt, ++gt) {
+                const int row = row_next;
+                if (lane < pages_per_tile && kt + 1 < u.n_kt) row_next = page_row(kt + 1);
                 const int st = gt % kStages;
                 uint8_t *ring = is_k ? s.k[st] : s.v[st];
                 if (lane == 0) {
@@ -290,29 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
                 if (!go) break;
                 if (lane < pages_per_tile) {
-                    const int lp = (u.kt0 + kt) * pages_per_tile + lane;
-                    const int row = lp < used_pages ? u.trow[lp] * ps : oob_row;
                     const uint32_t off = (uint32_t)lane * ps * 128;
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        if (csize == 1) {
-                            tma_load_3d(ring + j * kHalfBytes + off, tm, j * 64, u.kvh, row, &full[st]);
-                        } else if ((uint32_t)((2 * lane + j) % (int)csize) == crank) {
-                            tma_load_3d_multicast(ring + j * kHalfBytes + off, tm, j * 64, u.kvh, row, &full[st],
-                                                  cmask);
-                        }
+                        tma_load_3d(ring + j * kHalfBytes + off, tm, j * 64, u.kvh, row, &full[st]);
                     }
                 }
             }
         }
-        // With a cluster, peers release stages by remote arrivals: wait for the
-        // last ones so none lands after this CTA has exited.
-        if (go && csize > 1 && lane == 0) {
-            for (int t = max(0, gt - kStages); t < gt; ++t)
-                if (!mbar_wait(&empty[t % kStages], (t / kStages) & 1)) {
-                    set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
-                    break;
-                }
+        // Do not leave while a load of this warp may still be landing (only a
+        // timeout elsewhere can leave one unconsumed): wait, briefly, for the
+        // last tiles issued.
+        if (lane == 0) {
+            for (int t = gt - kStages > 0 ? gt - kStages : 0; t < gt; ++t)
+                mbar_wait(&full[t % kStages], (t / kStages) & 1, 2000000ll);
         }
     } else if (warp == 9 || warp == 11) {
         // ------------------------------------------------------ MMA issuers --
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int gt = 0;
             if (warp == 9) {
                 const uint32_t idesc_s = idesc_f16(kM, kN, prm.bf16 != 0, false, false);
-                const uint32_t q_addr = smem_u32(s.q);
+                const uint64_t q_desc = smem_desc(smem_u32(s.q), 16, 1024, kLayoutSwizzle128B);
                 for (int i = 0; ok && unit_of(i) < units; ++i) {
                     const Unit u = unit_at(unit_of(i));
                     if (!mbar_wait(&s.q_full, i & 1)) { ok = false; break; }
@@ -339,18 +339,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // the buffer's previous tile (gt-3) must be through its P.V (P lives in it)
                         if (gt >= 3 && !mbar_wait(&s.o_done[sb], ((gt / 3) - 1) & 1)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t k_addr = smem_u32(s.k[st]);
+                        // stage descriptors; a K-step adds its byte offset / 16 to the
+                        // start-address field (shared addresses are below 256 KB, so
+                        // the field never carries)
+                        const uint64_t k_desc = smem_desc(smem_u32(s.k[st]), 16, 1024, kLayoutSwizzle128B);
+                        const uint32_t d_s = tmem_s(sb);
+#pragma unroll
                         for (int ks = 0; ks < kD / 16; ++ks) {
-                            const uint32_t o = (ks / 4) * kHalfBytes + (ks % 4) * 32;
-                            mma_f16_ss(tmem_s(sb), smem_desc(q_addr + o, 16, 1024, kLayoutSwizzle128B),
-                                       smem_desc(k_addr + o, 16, 1024, kLayoutSwizzle128B), idesc_s,
-                                       ks > 0 ? 1u : 0u);
+                            const uint64_t o = (uint64_t)(((ks / 4) * kHalfBytes + (ks % 4) * 32) >> 4);
+                            mma_f16_ss(d_s, q_desc + o, k_desc + o, idesc_s, ks > 0 ? 1u : 0u);
                         }
                         mma_commit(&s.s_full[sb]);
-                        if (csize == 1)
-                            mma_commit(&s.k_empty[st]);
-                        else
-                            mma_commit_multicast(&s.k_empty[st], cmask);   // this CTA's copy of the K stage is free
+                        mma_commit(&s.k_empty[st]);
                     }
                     if (!ok) break;
                     mma_commit(&s.q_empty);        // Q is free once this unit's S MMAs are done
@@ -365,17 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!mbar_wait(&s.p_ready[gt % 3], (gt / 3) & 1)) { ok = false; break; }
                         if (!mbar_wait(&s.v_full[st], (gt / kStages) & 1)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t v_addr = smem_u32(s.v[st]);
+                        const uint64_t v_desc = smem_desc(smem_u32(s.v[st]), kHalfBytes, 1024, kLayoutSwizzle128B);
                         const uint32_t p_tmem = tmem_s(gt % 3);          // P (16-bit pairs) over the S columns
-                        for (int ks = 0; ks < kN / 16; ++ks) {
-                            const uint64_t b = smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, kLayoutSwizzle128B);
-                            mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
-                        }
+#pragma unroll
+                        for (int ks = 0; ks < kN / 16; ++ks)
+                            mma_f16_ts(tmem_o, p_tmem + ks * 8, v_desc + (uint64_t)((ks * 2048) >> 4), idesc_o,
+                                       (kt > 0 || ks > 0) ? 1u : 0u);
                         mma_commit(&s.o_done[gt % 3]);
-                        if (csize == 1)
-                            mma_commit(&s.v_empty[st]);
-                        else
-                            mma_commit_multicast(&s.v_empty[st], cmask);   // this CTA's copy of the V stage is free
+                        mma_commit(&s.v_empty[st]);
                     }
                 }
             }
@@ -574,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     griddep_launch();
     tc_fence_before();
-    cluster_barrier();
+    __syncthreads();
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -588,6 +585,31 @@ bool make_map(CUtensorMap *m, const void *base, int heads, int64_t rows, int box
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename T>
+cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &prm,
+                     int units, cudaStream_t st) {
+    // Persistent grid: no more CTAs than can be resident at once (one per SM;
+    // each walks its share of the units), so none waits for another to finish.
+    static int resident = 0;
+    if (resident == 0) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        int per_sm = 0, dev = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_kernel<T>, kThreads, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        resident = per_sm * sms > 0 ? per_sm * sms : 1;
+    }
+    const dim3 grid((unsigned)(units < resident ? units : resident));
+    cudaError_t e = launch_pdl(prefill_kernel<T>, grid, dim3(kThreads), kSmemBytes, st, tq, tk, tv, prm);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 }  // namespace
 
@@ -619,59 +641,10 @@ cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {
     prm.causal = a.causal;
     prm.window = a.window;
     prm.bf16 = bf16 ? 1 : 0;
-    // Cluster of 2 CTAs = query heads sharing one KV head (consecutive
-    // blocks: block = tile * Hq + head, and the group size divides Hq).
-    const int group = a.hq / a.hkv;
-    const unsigned csize = group % 2 == 0 ? 2u : 1u;
-    const int units = a.plan.n_tiles * a.splits * a.hq / (int)csize;
-    cudaLaunchConfig_t cfg{};
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // programmatic dependent launch
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    // Persistent grid: no more clusters than can be resident at once (each
-    // walks its share of the units), so none waits for another to finish.
-    auto launch = [&](auto kernel, int &resident, bool &configured) -> cudaError_t {
-        if (!configured) {
-            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-            if (e != cudaSuccess) return e;
-            int clusters = 0;
-            cfg.gridDim = dim3(csize * (unsigned)units);
-            e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
-            if (e != cudaSuccess || clusters < 1) {
-                int dev = 0, sms = 0;
-                cudaGetLastError();
-                if (cudaGetDevice(&dev) != cudaSuccess ||
-                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-                    return cudaErrorInvalidValue;
-                clusters = sms / (int)csize;
-            }
-            resident = clusters > 0 ? clusters : 1;
-            configured = true;
-        }
-        cfg.gridDim = dim3(csize * (unsigned)(units < resident ? units : resident));
-        return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, prm);
-    };
-    cudaError_t e;
-    if (bf16) {
-        static int resident[3] = {0, 0, 0};
-        static bool configured[3] = {false, false, false};
-        e = launch(prefill_kernel<__nv_bfloat16>, resident[csize], configured[csize]);
-    } else {
-        static int resident[3] = {0, 0, 0};
-        static bool configured[3] = {false, false, false};
-        e = launch(prefill_kernel<__half>, resident[csize], configured[csize]);
-    }
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    const int64_t units = (int64_t)a.plan.n_tiles * a.splits * a.hq;
+    if (units > INT32_MAX) return cudaErrorInvalidValue;
+    return bf16 ? launch_t<__nv_bfloat16>(tq, tk, tv, prm, (int)units, st)
+                : launch_t<__half>(tq, tk, tv, prm, (int)units, st);
 }
 
 }  // namespace pa
