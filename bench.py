@@ -606,10 +606,21 @@ def profile_run(args):
         case = workloads.long_context_decode_bf16()
     elif args.profile == "prefill":
         case = workloads.mixed_prefill_decode_bf16(n_prefill=n or 8, n_decode=0 if n else 120)
-    else:
+    elif args.profile == "mla":
         case = workloads.mla_decode_bf16(num_seqs=n or 128)
+    else:
+        # decode loop with the schedule advanced on the device each step: the GQA
+        # decode workload with pages reserved for the positions the loop reaches
+        base = workloads.gqa_decode_bf16(num_seqs=n or 64)
+        ctx = [int(x) for x in base.seq_lens]
+        grow = args.profile_iters + 2
+        case = workloads.build_case("gqa_decode_loop", base.meta["seed"], [x + grow for x in ctx],
+                                    [(i, x - 1) for i, x in enumerate(ctx)], base.hq, base.hkv, base.d, base.dv,
+                                    base.page_size, base.dtype, base.scale)
     step = DecodeStep(case, device, splits=args.splits)
     for _ in range(args.profile_iters):
+        if args.profile == "advance":
+            pka.paged_attn_plan_advance(step.plan)
         step.store()
         step.attend()
     torch.cuda.synchronize(device)
@@ -629,7 +640,7 @@ def main():
                     help="comma list of secondary workloads: long, gqa, mixed, mla ('' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--splits", type=int, default=None, help="override the split heuristic")
-    ap.add_argument("--profile", choices=["gqa", "long", "prefill", "mla"], default=None,
+    ap.add_argument("--profile", choices=["gqa", "long", "prefill", "mla", "advance"], default=None,
                     help="run a few un-timed steps of one workload (for ncu captures) and exit")
     ap.add_argument("--profile-seqs", type=int, default=0,
                     help="with --profile: number of sequences (0 = the full workload)")

@@ -24,14 +24,17 @@
 //      released as soon as that part of the score MMA has run;
 //   v: the CTA's own latent half, the K-major B operand of the rest of Q.K^T
 //      and the MN-major B operand (V) of P.V, released after P.V.
-// The MMA order per tile, S_w(t), P.V(t-1), S_v(t), gives the v ring's reload
-// for tile t+1 the time of S_v(t), S_w(t+1) and P.V(t) to land.  P (16-bit) is
-// written back over its row of the S buffer and read from TMEM by P.V; two
-// S/P buffers let the score MMA of the next tile run during this tile's softmax.
+// P (16-bit) is written back over its row of the S buffer and read from TMEM
+// by P.V; two S/P buffers let the score MMAs of the next tile run during this
+// tile's softmax.  One thread issues a tcgen05.mma only every ~100 cycles while
+// the tensor core finishes a 128 x 64 x 16 step in about half of that, so the
+// score MMAs of even and odd key tiles come from two threads (each into its
+// own S buffer and ring slot) and a third issues every P.V in order.
 //
 // Roles per CTA: warps 0-3 softmax/epilogue (thread r = head r, TMEM lane r),
-// warp 4 TMA producer of Q and the w ring, warp 5 MMA issuer, warp 6 TMA
-// producer of the v ring.  Key tiles are 64 keys, one page at page_size 64
+// warp 4 TMA producer of Q and the w ring, warps 5 and 7 score-MMA issuers
+// (even / odd key tiles), warp 6 TMA producer of the v ring, warp 8 P.V
+// issuer.  Key tiles are 64 keys, one page at page_size 64
 // (several boxes for smaller pages).  Keys at or past the visible end score
 // -inf and their latent rows are zeroed before P.V (tail slots may hold
 // anything).  All waits are bounded (timeout -> device status word).
@@ -53,7 +56,8 @@ constexpr int kHeads = 128;               // M: heads per CTA (TMEM lanes)
 constexpr int kR = 512;                   // latent rank
 constexpr int kP = 64;                    // rotary position dims
 constexpr int kN = 64;                    // keys per tile
-constexpr int kThreads = 224;             // 4 softmax + w producer + MMA + v producer
+constexpr int kThreads = 288;             // 4 softmax + w producer + score MMA (even tiles) + v producer
+                                          // + score MMA (odd tiles) + P.V MMA
 constexpr int kBlk = kHeads * 128;        // one 64-column block of the Q tile (bytes)
 constexpr int kKBlk = kN * 128;           // one 64-column block of a key tile (bytes)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -220,55 +224,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 5) {
-        // ------------------------------------------------------ MMA issuer --
+    } else if (warp == 5 || warp == 7) {
+        // ------------------------------------------------ score MMA issuers --
+        // A thread issues a tcgen05.mma only every ~100 cycles, so a 64-key
+        // tile's 36 score MMAs (20 with Q from shared memory, 16 with the own
+        // latent half of Q from TMEM) take one thread three times as long as
+        // the tensor core needs for them.  Warp 5 issues the scores of the even
+        // key tiles into S buffer 0, warp 7 those of the odd tiles into buffer
+        // 1; warp 8 issues every P.V.  A buffer is written again only once the
+        // P.V of the tile before has read its P (o_done).
         if (lane == 0) {
+            const int par = warp == 5 ? 0 : 1;              // tiles kt with kt % 2 == par, ring slot par
             const uint32_t idesc_s = idesc_f16(kHeads, kN, prm.bf16 != 0, false, false);
-            const uint32_t idesc_o = idesc_f16(kHeads, 256, prm.bf16 != 0, false, true);
             bool ok = mbar_wait(&s.q_full, 0) && mbar_wait(&s.q_ready, 0);
-            auto issue_pv = [&](int kt) -> bool {
-                if (!mbar_wait(&s.p_ready[kt & 1], (kt / 2) & 1)) return false;
-                tc_fence_after();
-                const int slot = kt & 1;
-                const uint32_t v_addr = smem_u32(s.v[slot][0]);
-                const uint32_t p_tmem = tmem_s(kt & 1);           // P (16-bit pairs) over the S columns
-                for (int ks = 0; ks < kN / 16; ++ks) {
-                    const uint64_t b = smem_desc(v_addr + ks * 2048, kKBlk, 1024, kLayoutSwizzle128B);
-                    mma_f16_ts(tmem_o, p_tmem + ks * 8, b, idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
-                }
-                mma_commit(&s.o_done[kt & 1]);
-                mma_commit(&s.v_empty[slot]);
-                return true;
-            };
-            for (int kt = 0; ok && kt < n_kt; ++kt) {
-                const int slot = kt & 1, sb = kt & 1;
-                if (!mbar_wait(&s.w_full[slot], (kt / 2) & 1)) { ok = false; break; }
+            const uint32_t d_s = tmem_s(par);
+            // descriptors of the operand bases; a K-step adds its byte offset / 16
+            // to the start-address field (shared addresses stay below 256 KB)
+            uint64_t qd[5];
+#pragma unroll
+            for (int blk = 0; blk < 5; ++blk) qd[blk] = smem_desc(smem_u32(s.q[blk]), 16, 1024, kLayoutSwizzle128B);
+            for (int kt = par; ok && kt < n_kt; kt += 2) {
+                const uint32_t ph = (uint32_t)(kt / 2) & 1u;
+                if (!mbar_wait(&s.w_full[par], ph)) { ok = false; break; }
                 // the buffer's previous tile (kt-2) must be through its P.V (P lives in it)
-                if (kt >= 2 && !mbar_wait(&s.o_done[sb], ((kt / 2) - 1) & 1)) { ok = false; break; }
+                if (kt >= 2 && !mbar_wait(&s.o_done[par], ph ^ 1u)) { ok = false; break; }
                 tc_fence_after();
                 // peer latent half and position columns: A (Q) from shared memory
-                for (int blk = 0; blk < 5; ++blk)
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t a = smem_desc(smem_u32(s.q[blk]) + k * 32, 16, 1024, kLayoutSwizzle128B);
-                        const uint64_t b = smem_desc(smem_u32(s.w[slot][blk]) + k * 32, 16, 1024, kLayoutSwizzle128B);
-                        mma_f16_ss(tmem_s(sb), a, b, idesc_s, (blk > 0 || k > 0) ? 1u : 0u);
-                    }
-                mma_commit(&s.w_empty[slot]);
-                if (kt > 0 && !issue_pv(kt - 1)) { ok = false; break; }
-                if (!mbar_wait(&s.v_full[slot], (kt / 2) & 1)) { ok = false; break; }
+#pragma unroll
+                for (int blk = 0; blk < 5; ++blk) {
+                    const uint64_t wd = smem_desc(smem_u32(s.w[par][blk]), 16, 1024, kLayoutSwizzle128B);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16_ss(d_s, qd[blk] + (uint64_t)(k * 2), wd + (uint64_t)(k * 2), idesc_s,
+                                   (blk > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(&s.w_empty[par]);
+                if (!mbar_wait(&s.v_full[par], ph)) { ok = false; break; }
                 tc_fence_after();
                 // own latent half: A (Q) from TMEM
-                for (int blk = 0; blk < 4; ++blk)
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t b = smem_desc(smem_u32(s.v[slot][blk]) + k * 32, 16, 1024, kLayoutSwizzle128B);
-                        mma_f16_ts(tmem_s(sb), tmem_q + blk * 32 + k * 8, b, idesc_s, 1u);
-                    }
-                mma_commit(&s.s_full[sb]);
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+                    const uint64_t vd = smem_desc(smem_u32(s.v[par][blk]), 16, 1024, kLayoutSwizzle128B);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16_ts(d_s, tmem_q + blk * 32 + k * 8, vd + (uint64_t)(k * 2), idesc_s, 1u);
+                }
+                mma_commit(&s.s_full[par]);
             }
-            if (ok && n_kt > 0) ok = issue_pv(n_kt - 1);
             if (!ok) atomicCAS(prm.status, 0, PA_DEVICE_TIMEOUT_MMA);
         }
-    } else {
+    } else if (warp == 8) {
+        // ------------------------------------------------------ P.V issuer --
+        // O += P V for every key tile in order (one accumulator, one thread).
+        // S of the tile has completed before its P exists, so the v stage that
+        // both the score and this MMA read is free once this MMA has run.
+        if (lane == 0) {
+            const uint32_t idesc_o = idesc_f16(kHeads, 256, prm.bf16 != 0, false, true);
+            bool ok = true;
+            for (int kt = 0; ok && kt < n_kt; ++kt) {
+                const int slot = kt & 1;
+                const uint32_t ph = (uint32_t)(kt / 2) & 1u;
+                if (!mbar_wait(&s.p_ready[slot], ph) || !mbar_wait(&s.v_full[slot], ph)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t vd = smem_desc(smem_u32(s.v[slot][0]), kKBlk, 1024, kLayoutSwizzle128B);
+                const uint32_t p_tmem = tmem_s(slot);           // P (16-bit pairs) over the S columns
+#pragma unroll
+                for (int ks = 0; ks < kN / 16; ++ks)
+                    mma_f16_ts(tmem_o, p_tmem + ks * 8, vd + (uint64_t)((ks * 2048) >> 4), idesc_o,
+                               (kt > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(&s.o_done[slot]);
+                mma_commit(&s.v_empty[slot]);
+            }
+            if (!ok) atomicCAS(prm.status, 0, PA_DEVICE_TIMEOUT_MMA);
+        }
+    } else if (warp < 4) {
         // ---------------------------------------- softmax / epilogue rows --
         const int r = tid;
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
