@@ -369,6 +369,61 @@ def e2e_leg(case, device, steps: int, warmup: int):
     return res
 
 
+def e2e_static_leg(case, device, steps: int, warmup: int):
+    """The mixed prefill + decode call end to end through the public API with host
+    buffers: one CUDA graph holds the pinned host-to-device copies of the step's
+    q and new K/V rows, the append, the attention (prefill tiles and decode
+    items) and the device-to-host copy of the output; per step the host replays
+    it and waits.  The schedule is uploaded once (a serving step would stage a
+    new one with pa_plan_stage, which a graph can hold as well); every step
+    appends the same rows at the same positions, so the flops per step are the
+    workload's.  The last replay is checked against the same attention called
+    directly."""
+    import paged_kv_attention_20_gb300 as pka
+    step = DecodeStep(case, device)
+    names = ("q", "new_k", "new_v")
+    host = {k: getattr(case, k).pin_memory() for k in names}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def body():
+        for k in names:
+            getattr(step.dc, k).copy_(host[k], non_blocking=True)
+        step.store()
+        step.attend()
+        out_host.copy_(step.out, non_blocking=True)
+
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        body()                       # kernel attributes are set outside capture
+    torch.cuda.current_stream(device).wait_stream(side)
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        graph.replay()
+        stream.synchronize()
+    t = time.perf_counter()
+    for _ in range(steps):
+        graph.replay()
+        stream.synchronize()
+    dt = time.perf_counter() - t
+    last = out_host.clone()
+    step.attend()
+    torch.cuda.synchronize(device)
+    if not torch.equal(step.out.cpu(), last) or pka.device_status() != 0:
+        raise RuntimeError("graph-replayed mixed step differs from the direct call")
+    fl = attn_flops(case)
+    return {"value": fl * steps / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": dt / steps * 1e3, "splits": step.splits,
+            "mode": "per step one CUDA graph replay: pinned H2D of q, new_k, new_v; paged_kv_store; "
+                    "paged_attn_forward_split (prefill tiles + decode items); D2H of the output; host wait"}
+
+
 DECODE_ONLY = ("long", "gqa")
 
 
@@ -438,6 +493,7 @@ def secondary(device, warmup: int, steps: int, peaks, which, cpu=True):
                              prefill_kernel_frac_bf16_peak=pfl / kms / 1e9 / tc,
                              decode_kv_bytes=kv_bytes(case, npq), note="ms and tflops cover the whole call: the "
                              "prefill kernel, then the decode items (HBM-bound)")
+            res[name]["e2e"] = e2e_static_leg(case, device, steps=max(10, steps), warmup=warmup)
         if cpu:
             label = "MLA decode workload" if case.is_mla else "mixed prefill + decode workload"
             res[name]["cpu_baseline"] = cpu_baseline(case, label, unit="TFLOP/s")
