@@ -289,17 +289,100 @@ def soak_clocks(step: DecodeStep, device, seconds=1.0):
     return c
 
 
+def _pipelined_e2e(step, names, host_src, device, steps: int, warmup: int, pre=None):
+    """Replays a step through the public API from host buffers, software-
+    pipelined as a serving loop runs it.  Two CUDA graphs alternate.  Graph p
+    runs `pre` (if any), paged_kv_store and the attention on device input set
+    p into device output p; beside it, on a second stream, it copies the next
+    step's inputs from pinned host set 1-p into device set 1-p and the
+    previous step's output from device output 1-p into pinned host buffer 1-p.
+    The host enqueues step i+1, then waits for step i.  Every step thus moves
+    one step's inputs host-to-device and one output device-to-host, and both
+    copies overlap a step's kernels; the timed region ends with the copy of
+    the last step's output.  Returns (seconds for `steps` steps, the last
+    output on the host)."""
+    import copy
+    base = step.dc
+    dsets = [base, copy.copy(base)]
+    for k in names:
+        setattr(dsets[1], k, getattr(base, k).clone())
+    douts = [step.out, torch.empty_like(step.out)]
+    hsets = [{k: host_src[k].pin_memory() for k in names} for _ in range(2)]
+    outs = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
+    stream = torch.cuda.current_stream(device)
+    copier = torch.cuda.Stream(device)
+
+    def body(p):
+        cur = torch.cuda.current_stream(device)
+        copier.wait_stream(cur)
+        with torch.cuda.stream(copier):
+            for k in names:
+                getattr(dsets[1 - p], k).copy_(hsets[1 - p][k], non_blocking=True)
+            outs[1 - p].copy_(douts[1 - p], non_blocking=True)
+        step.dc, step.out = dsets[p], douts[p]
+        if pre:
+            pre()
+        step.store()
+        step.attend()
+        cur.wait_stream(copier)
+
+    side = torch.cuda.Stream(device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for k in names:
+            getattr(dsets[0], k).copy_(hsets[0][k], non_blocking=True)
+        body(0)                      # kernel attributes are set outside capture (first `pre`)
+    stream.wait_stream(side)
+    torch.cuda.synchronize(device)
+    graphs = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
+    for p in range(2):
+        with torch.cuda.graph(graphs[p]):
+            body(p)
+    evs = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def run(n, first):
+        if n == 0:
+            return first
+        prev = None
+        for i in range(n):
+            p = (first + i) % 2
+            graphs[p].replay()
+            evs[p].record(stream)
+            if prev is not None:
+                evs[prev].synchronize()      # step i-1 done (and step i-2's output on the host)
+            prev = p
+        evs[prev].synchronize()
+        return (prev + 1) % 2
+
+    nxt = run(warmup, 1)             # the eager step used set 0 and filled set 1
+    last = (nxt + 1) % 2
+    t = time.perf_counter()
+    nxt = run(steps, nxt)
+    last = (nxt + 1) % 2
+    outs[last].copy_(douts[last], non_blocking=True)
+    stream.synchronize()
+    dt = time.perf_counter() - t
+    step.dc, step.out = dsets[last], douts[last]
+    return dt, outs[last].clone()
+
+
+PIPELINE_MODE = ("two CUDA graphs alternate; graph p runs the step on device set p while a second stream "
+                 "copies the next step's inputs from pinned host set 1-p and the previous step's output "
+                 "into pinned host buffer 1-p; the host enqueues step i+1 before waiting for step i; the "
+                 "timed region ends with the copy of the last output")
+
+
 def e2e_leg(case, device, steps: int, warmup: int):
     """Same metric through the public API with host buffers, run as a decode
-    loop replays its attention layer: one CUDA graph holds the pinned host-to-
-    device copy of the step's inputs (q, the position query for MLA, and the new
-    cache rows), pa_plan_advance (every query moves one position on, on the
-    device), the append, the attention (split GQA, or MLA) and the device-to-host
-    copy of the output; per step the host replays it and waits.  The case is the
-    given decode workload with its pages reserved for the positions the loop
-    reaches; the KV bytes (and, for MLA, the flops) are counted per step as the
-    histories grow.  The last replay is checked against the same attention
-    called directly."""
+    loop replays its attention layer: each step copies its inputs (q, the
+    position query for MLA, and the new cache rows) from pinned host memory,
+    runs pa_plan_advance (every query moves one position on, on the device),
+    the append and the attention (split GQA, or MLA), and copies the output
+    back to pinned host memory; steps are software-pipelined (_pipelined_e2e).
+    The case is the given decode workload with its pages reserved for the
+    positions the loop reaches; the KV bytes (and, for MLA, the flops) are
+    counted per step as the histories grow.  The last step is checked against
+    the same attention called directly."""
     import workloads
     import paged_kv_attention_20_gb300 as pka
     total = warmup + steps + 2
@@ -310,41 +393,12 @@ def e2e_leg(case, device, steps: int, warmup: int):
                                  mla_p=case.p)
     step = DecodeStep(grown, device)
     names = ("q", "qp", "new_k", "new_v") if grown.is_mla else ("q", "new_k", "new_v")
-    host = {k: getattr(grown, k).pin_memory() for k in names}
-    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
-
-    def body():
-        for k in names:
-            getattr(step.dc, k).copy_(host[k], non_blocking=True)
-        pka.paged_attn_plan_advance(step.plan)
-        step.store()
-        step.attend()
-        out_host.copy_(step.out, non_blocking=True)
-
-    side = torch.cuda.Stream(device)
-    side.wait_stream(torch.cuda.current_stream(device))
-    with torch.cuda.stream(side):
-        body()                       # kernel attributes are set outside capture (first advance)
-    torch.cuda.current_stream(device).wait_stream(side)
-    torch.cuda.synchronize(device)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        body()
-    stream = torch.cuda.current_stream(device)
-
-    def one():
-        graph.replay()
-        stream.synchronize()
-
-    for _ in range(warmup):
-        one()
+    src = {k: getattr(grown, k) for k in names}
+    h2d = sum(t.numel() * t.element_size() for t in src.values())
+    d2h = step.out.numel() * step.out.element_size()
+    dt, last = _pipelined_e2e(step, names, src, device, steps, warmup,
+                              pre=lambda: pka.paged_attn_plan_advance(step.plan))
     done = 1 + warmup                # advances so far (the eager step and the warm-up replays)
-    t = time.perf_counter()
-    for _ in range(steps):
-        one()
-    dt = time.perf_counter() - t
     # positions during timed step i: ctx - 1 + done + 1 + i; keys seen: that + 1
     elt = grown.new_k.element_size()
     if grown.is_mla:
@@ -354,65 +408,37 @@ def e2e_leg(case, device, steps: int, warmup: int):
         per_tok = grown.hkv * (grown.d + grown.dv) * elt
         per_key_flops = grown.hq * (2 * grown.d + 2 * grown.dv)
     keys = sum(sum(ctx) + len(ctx) * (done + 1 + i) for i in range(steps))
-    last = out_host.clone()
-    step.attend()                    # the same attention on the state the last replay left
+    step.attend()                    # the same attention on the state the last step left
     torch.cuda.synchronize(device)
     if not torch.equal(step.out.cpu(), last) or pka.device_status() != 0:
         raise RuntimeError("graph-replayed decode step differs from the direct call")
     what = "paged_mla_forward" if grown.is_mla else "paged_attn_forward_split"
     res = {"value": keys * per_tok / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h), "ms_per_step": dt / steps * 1e3, "splits": step.splits,
-           "mode": f"per step one CUDA graph replay: pinned H2D of {', '.join(names)}; pa_plan_advance "
-                   f"(schedule on the device); paged_kv_store; {what}; D2H of the output; host wait"}
+           "mode": f"per step: pinned H2D of {', '.join(names)}; pa_plan_advance (schedule on the device); "
+                   f"paged_kv_store; {what}; D2H of the output into pinned memory; {PIPELINE_MODE}"}
     if grown.is_mla:
         res.update(value=keys * per_key_flops / dt / 1e12, unit="TFLOP/s", kv_gbs=keys * per_tok / dt / 1e9)
     return res
 
 
 def e2e_static_leg(case, device, steps: int, warmup: int):
-    """The mixed prefill + decode call end to end through the public API with host
-    buffers: one CUDA graph holds the pinned host-to-device copies of the step's
-    q and new K/V rows, the append, the attention (prefill tiles and decode
-    items) and the device-to-host copy of the output; per step the host replays
-    it and waits.  The schedule is uploaded once (a serving step would stage a
-    new one with pa_plan_stage, which a graph can hold as well); every step
-    appends the same rows at the same positions, so the flops per step are the
-    workload's.  The last replay is checked against the same attention called
-    directly."""
+    """The mixed prefill + decode call end to end through the public API with
+    host buffers: each step copies its q and new K/V rows from pinned host
+    memory, runs the append and the attention (prefill tiles and decode items)
+    and copies the output back to pinned host memory; steps are software-
+    pipelined (_pipelined_e2e).  The schedule is uploaded once (a serving step
+    would stage a new one with pa_plan_stage, which a graph can hold as well);
+    every step appends the same rows at the same positions, so the flops per
+    step are the workload's.  The last step is checked against the same
+    attention called directly."""
     import paged_kv_attention_20_gb300 as pka
     step = DecodeStep(case, device)
     names = ("q", "new_k", "new_v")
-    host = {k: getattr(case, k).pin_memory() for k in names}
-    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
-
-    def body():
-        for k in names:
-            getattr(step.dc, k).copy_(host[k], non_blocking=True)
-        step.store()
-        step.attend()
-        out_host.copy_(step.out, non_blocking=True)
-
-    side = torch.cuda.Stream(device)
-    side.wait_stream(torch.cuda.current_stream(device))
-    with torch.cuda.stream(side):
-        body()                       # kernel attributes are set outside capture
-    torch.cuda.current_stream(device).wait_stream(side)
-    torch.cuda.synchronize(device)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        body()
-    stream = torch.cuda.current_stream(device)
-    for _ in range(warmup):
-        graph.replay()
-        stream.synchronize()
-    t = time.perf_counter()
-    for _ in range(steps):
-        graph.replay()
-        stream.synchronize()
-    dt = time.perf_counter() - t
-    last = out_host.clone()
+    src = {k: getattr(case, k) for k in names}
+    h2d = sum(t.numel() * t.element_size() for t in src.values())
+    d2h = step.out.numel() * step.out.element_size()
+    dt, last = _pipelined_e2e(step, names, src, device, steps, warmup)
     step.attend()
     torch.cuda.synchronize(device)
     if not torch.equal(step.out.cpu(), last) or pka.device_status() != 0:
@@ -420,8 +446,8 @@ def e2e_static_leg(case, device, steps: int, warmup: int):
     fl = attn_flops(case)
     return {"value": fl * steps / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": dt / steps * 1e3, "splits": step.splits,
-            "mode": "per step one CUDA graph replay: pinned H2D of q, new_k, new_v; paged_kv_store; "
-                    "paged_attn_forward_split (prefill tiles + decode items); D2H of the output; host wait"}
+            "mode": "per step: pinned H2D of q, new_k, new_v; paged_kv_store; paged_attn_forward_split "
+                    f"(prefill tiles + decode items); D2H of the output into pinned memory; {PIPELINE_MODE}"}
 
 
 DECODE_ONLY = ("long", "gqa")
@@ -485,14 +511,29 @@ def secondary(device, warmup: int, steps: int, peaks, which, cpu=True):
                              kv_gbs=kv_bytes(case) / ms / 1e6, frac_hbm=kv_bytes(case) / ms / 1e6 / hbm)
             res[name]["e2e"] = e2e_leg(case, device, steps=max(10, steps), warmup=warmup)
         else:
-            # prefill chunks are the first n_prefill * chunk queries; their kernel is timed alone
-            # (the call then runs the decode items, an HBM-bound kernel, after it)
+            # prefill chunks are the first n_prefill * chunk queries.  In the call the decode items
+            # (HBM-bound) run beside the prefill kernel on a share of the SMs, so the prefill
+            # kernel is also timed alone, on the whole GPU, over a plan of the same chunks only
             npq = case.meta["n_prefill"] * case.meta["chunk"]
             pfl = attn_flops(case, 0, npq)
-            res[name].update(prefill_kernel_ms=kms, prefill_flops=pfl, prefill_kernel_tflops=pfl / kms / 1e9,
-                             prefill_kernel_frac_bf16_peak=pfl / kms / 1e9 / tc,
-                             decode_kv_bytes=kv_bytes(case, npq), note="ms and tflops cover the whole call: the "
-                             "prefill kernel, then the decode items (HBM-bound)")
+            pcase = maker(n_decode=0)
+            pst = DecodeStep(pcase, device)
+            for _ in range(warmup):
+                pst.attend()
+            pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for i in range(steps):
+                pst.pka.time_next_kernel(*pev[i])
+                pst.attend()
+            torch.cuda.synchronize(device)
+            pkms = sum(a.elapsed_time(b) for a, b in pev) / steps
+            del pst, pcase
+            res[name].update(prefill_kernel_ms=pkms, prefill_flops=pfl, prefill_kernel_tflops=pfl / pkms / 1e9,
+                             prefill_kernel_frac_bf16_peak=pfl / pkms / 1e9 / tc,
+                             prefill_kernel_ms_in_call=kms, decode_kv_bytes=kv_bytes(case, npq),
+                             note="ms and tflops cover the whole call: the prefill kernel with the decode items "
+                                  "(HBM-bound) beside it on a share of the SMs; prefill_kernel_* is the prefill "
+                                  "kernel alone on the whole GPU over the same chunks (a plan without the decode "
+                                  "items), prefill_kernel_ms_in_call the same kernel inside the mixed call")
             res[name]["e2e"] = e2e_static_leg(case, device, steps=max(10, steps), warmup=warmup)
         if cpu:
             label = "MLA decode workload" if case.is_mla else "mixed prefill + decode workload"

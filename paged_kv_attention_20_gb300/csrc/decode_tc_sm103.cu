@@ -548,7 +548,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 template <typename T, int CW>
 cudaError_t launch_cw(const AttnArgs &a, int items, int use_list, const CUtensorMap &tk, const CUtensorMap &tv,
                       const TcParams &tp, cudaStream_t st) {
-    // Persistent grid: as many CTAs as fit on the GPU at once (one per SM).
+    // Persistent grid: as many CTAs as fit on the GPU at once (one per SM), or
+    // fewer when the caller keeps SMs for a concurrent kernel.
     static int resident = 0;
     if (resident == 0) {
         cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<T, CW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -564,7 +565,9 @@ cudaError_t launch_cw(const AttnArgs &a, int items, int use_list, const CUtensor
         resident = per_sm * sms > 0 ? per_sm * sms : 1;
     }
     const int64_t units = (int64_t)items * a.splits * a.hkv;
-    const dim3 grid((unsigned)(units < resident ? units : resident));
+    int64_t ctas = units < resident ? units : resident;
+    if (a.max_ctas > 0 && a.max_ctas < ctas) ctas = a.max_ctas;
+    const dim3 grid((unsigned)ctas);
     cudaError_t e = launch_pdl(decode_tc_kernel<T, CW>, grid, dim3(kThreads), kSmemBytes, st, tk, tv, a, use_list, tp);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -49,6 +49,7 @@ struct AttnArgs {
     int32_t splits;
     pa_dtype dtype;
     int32_t *status;      // device status word (bounded waits record timeouts here)
+    int32_t max_ctas;     // persistent kernels: at most this many CTAs (0: as many as are resident at once)
 };
 
 // Keys a query at absolute position `pos` of a sequence holding `seq_len`

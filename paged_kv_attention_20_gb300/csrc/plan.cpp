@@ -48,6 +48,50 @@ bool valid_dtype(pa_dtype d) { return d == PA_F32 || d == PA_F16 || d == PA_BF16
 
 int elem_bytes(pa_dtype d) { return d == PA_F32 ? 4 : 2; }
 
+// A mixed call's decode items can run beside its prefill tiles: the tiles are
+// bound by the tensor core and the softmax, the decode items by HBM, and one
+// after the other they leave one of the two idle for the whole of the other.
+// The decode kernel then runs on a second stream of the caller's thread (one
+// per device, created on first use outside stream capture), forked from and
+// joined back into the caller's stream with events, so the call stays one
+// ordered step of that stream and can be captured into a graph.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool failed = false;
+};
+
+constexpr int kMaxSideDevices = 64;
+
+SideStream *side_stream(cudaStream_t st) {
+    thread_local SideStream side[kMaxSideDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return nullptr;
+    SideStream &ss = side[dev];
+    if (ss.stream) return &ss;
+    if (ss.failed) return nullptr;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
+    if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+        (void)cudaGetLastError();
+        ss.failed = true;
+        ss.stream = nullptr;
+        return nullptr;
+    }
+    return &ss;
+}
+
+int device_sms() {
+    static int sms[kMaxSideDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return 0;
+    if (sms[dev] == 0 && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms[dev];
+}
+
 pa::PlanView view_of(const pa_plan *p) {
     pa::PlanView v{};
     v.qmeta = reinterpret_cast<const int4 *>(p->dev + p->off_qmeta);
@@ -435,6 +479,51 @@ pa_status pa::check_attention_args(const pa_plan *plan, int32_t hq, int32_t hkv,
 namespace {
 
 // Shared body of the attention entry points.
+// SMs to leave to the decode items of a mixed call while its prefill tiles
+// run on the others (0: run them one after the other).  Model, from runs of
+// the mixed workload on GB300 (128-wide heads): the prefill kernel does
+// kPrefillFlopsPerSm on each of its SMs; while it runs, the decode kernel
+// reads kDecodeBytesPerSm on each of its own SMs but no more than
+// kDecodeBesidePrefill in all (the prefill's own loads share HBM and L2);
+// what is left of the decode then runs on the whole GPU at kHbmBytes.  The
+// share with the shortest modelled call is taken when it saves at least 5 %
+// and both halves are long enough for the fork and join to be noise.
+int decode_sms_beside_prefill(const pa_plan *plan, const pa::AttnArgs &a, int sms) {
+    constexpr double kPrefillFlopsPerSm = 6.5e12, kDecodeBytesPerSm = 7.2e10, kDecodeBesidePrefill = 2.0e12,
+                     kHbmBytes = 6.2e12;
+    if (plan->n_decode == 0 || plan->n_tiles == 0 || sms < 8) return 0;
+    const int32_t *w = plan->words.data();
+    auto visible = [&](int q) -> double {
+        const int seq = w[plan->off_qmeta + 4 * (size_t)q], pos = w[plan->off_qmeta + 4 * (size_t)q + 1];
+        int64_t lo, hi;
+        pa::visible_range(pos, w[plan->off_seqlen + seq], a.causal, a.window, lo, hi);
+        return (double)(hi > lo ? hi - lo : 0);
+    };
+    double keys_p = 0, keys_d = 0;
+    for (int t = 0; t < plan->n_tiles; ++t) {
+        const int32_t *tile = w + plan->off_tiles + 4 * (size_t)t;
+        for (int i = 0; i < tile[2]; ++i) keys_p += visible(tile[1] + i);
+    }
+    for (int i = 0; i < plan->n_decode; ++i) keys_d += visible(w[plan->off_decode + i]);
+    const double flops = keys_p * a.hq * 2.0 * (a.d + a.dv);
+    const double bytes = keys_d * a.hkv * (double)(a.d + a.dv) * elem_bytes(a.dtype);
+    const double t_prefill = flops / (kPrefillFlopsPerSm * sms), t_decode = bytes / kHbmBytes;
+    if (t_prefill < 20e-6 || t_decode < 20e-6) return 0;
+    const double serial = t_prefill + t_decode;
+    double best = serial;
+    int best_n = 0;
+    for (int n = 1; n < sms / 2; ++n) {
+        const double tp = flops / (kPrefillFlopsPerSm * (sms - n));
+        const double beside = std::min(kDecodeBesidePrefill, kDecodeBytesPerSm * n) * tp;
+        const double t = bytes > beside ? tp + (bytes - beside) / kHbmBytes : std::max(tp, bytes / kHbmBytes);
+        if (t < best) {
+            best = t;
+            best_n = n;
+        }
+    }
+    return best < 0.95 * serial ? best_n : 0;
+}
+
 pa_status attention(const pa_plan *plan, const void *q, const void *k, const void *v, const void *qp,
                     const void *kp, void *out, int32_t hq, int32_t hkv, int32_t d, int32_t dv, int32_t p,
                     float scale, int32_t causal, int32_t window, pa_dtype dtype, void *ws, size_t ws_bytes, int32_t splits,
@@ -499,10 +588,30 @@ pa_status attention(const pa_plan *plan, const void *q, const void *k, const voi
         bool tiles = plan->n_tiles > 0 && pa::prefill_supported(a);
         if (tiles) {
             // with splits > 1 both kernels write partials and one merge covers every query
-            mark(t0);
-            e = pa::launch_prefill(a, st);
-            mark(t1);
-            if (e == cudaSuccess && plan->n_decode > 0) e = pa::launch_decode(a, true, st);
+            const int sms = device_sms();
+            const int beside = sms > 0 ? decode_sms_beside_prefill(plan, a, sms) : 0;
+            SideStream *side = beside > 0 ? side_stream(st) : nullptr;
+            if (side) {
+                // prefill on sms - beside persistent CTAs, launched first so that they
+                // hold their SMs; the decode items fill the rest from the side stream
+                e = cudaEventRecord(side->fork, st);
+                if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+                pa::AttnArgs ap = a;
+                ap.max_ctas = sms - beside;
+                mark(t0);
+                if (e == cudaSuccess) e = pa::launch_prefill(ap, st);
+                mark(t1);
+                pa::AttnArgs ad = a;
+                ad.max_ctas = beside;
+                if (e == cudaSuccess) e = pa::launch_decode(ad, true, side->stream);
+                if (e == cudaSuccess) e = cudaEventRecord(side->join, side->stream);
+                if (e == cudaSuccess) e = cudaStreamWaitEvent(st, side->join, 0);
+            } else {
+                mark(t0);
+                e = pa::launch_prefill(a, st);
+                mark(t1);
+                if (e == cudaSuccess && plan->n_decode > 0) e = pa::launch_decode(a, true, st);
+            }
             if (e == cudaSuccess && splits > 1) e = pa::launch_merge(a, false, st);
         } else {
             // every query is a decode item: use the (longest-first) decode list

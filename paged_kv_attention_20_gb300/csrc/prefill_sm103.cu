@@ -588,9 +588,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 template <typename T>
 cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &prm,
-                     int units, cudaStream_t st) {
+                     int units, int max_ctas, cudaStream_t st) {
     // Persistent grid: no more CTAs than can be resident at once (one per SM;
-    // each walks its share of the units), so none waits for another to finish.
+    // each walks its share of the units), so none waits for another to finish;
+    // fewer when the caller keeps SMs free for a concurrent kernel.
     static int resident = 0;
     if (resident == 0) {
         cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -605,7 +606,9 @@ cudaError_t launch_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtenso
         if (e != cudaSuccess) return e;
         resident = per_sm * sms > 0 ? per_sm * sms : 1;
     }
-    const dim3 grid((unsigned)(units < resident ? units : resident));
+    int ctas = units < resident ? units : resident;
+    if (max_ctas > 0 && max_ctas < ctas) ctas = max_ctas;
+    const dim3 grid((unsigned)ctas);
     cudaError_t e = launch_pdl(prefill_kernel<T>, grid, dim3(kThreads), kSmemBytes, st, tq, tk, tv, prm);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -643,8 +646,8 @@ cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t st) {
     prm.bf16 = bf16 ? 1 : 0;
     const int64_t units = (int64_t)a.plan.n_tiles * a.splits * a.hq;
     if (units > INT32_MAX) return cudaErrorInvalidValue;
-    return bf16 ? launch_t<__nv_bfloat16>(tq, tk, tv, prm, (int)units, st)
-                : launch_t<__half>(tq, tk, tv, prm, (int)units, st);
+    return bf16 ? launch_t<__nv_bfloat16>(tq, tk, tv, prm, (int)units, a.max_ctas, st)
+                : launch_t<__half>(tq, tk, tv, prm, (int)units, a.max_ctas, st);
 }
 
 }  // namespace pa
