@@ -9,6 +9,7 @@ while the caller's stream is being captured, on a thread that has no second
 stream yet, runs the two kernels one after the other instead.  Every form must
 give the same output, bit for bit, and that output must match the oracle.
 """
+import math
 import threading
 
 import numpy as np
@@ -17,7 +18,7 @@ import torch
 
 import paged_kv_attention_20_gb300 as pka
 from helpers import assert_close, oracle_after_store
-from workloads import mixed_prefill_decode_bf16
+from workloads import build_case, mixed_prefill_decode_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -121,3 +122,56 @@ def test_mixed_call_split_workspace_same_bits(cuda_device):
     ref, _, _, _ = oracle_after_store(case, rows=rows)
     got = outs[0].double().cpu().numpy().reshape(-1, case.dv)[rows]
     assert_close(got, ref, case.dtype, "mixed split call beside")
+
+
+def test_mixed_call_tensor_core_decode_beside(cuda_device):
+    # groups of 8 query heads per KV head: the decode items run on the persistent
+    # tensor-core decode kernel, its grid capped to the SMs the prefill leaves
+    gen = np.random.default_rng(31)
+    offs = [int(x) for x in gen.integers(1024, 3072, size=4)]
+    dctx = [int(x) for x in gen.integers(2048, 6144, size=64)]
+    chunk = 512
+    seq_lens = [o + chunk for o in offs] + dctx
+    queries = [(s, o + i) for s, o in enumerate(offs) for i in range(chunk)]
+    queries += [(len(offs) + s, n - 1) for s, n in enumerate(dctx)]
+    case = build_case("mixed_g8", 37, seq_lens, queries, 64, 8, 128, 128, 16, torch.bfloat16, 1 / math.sqrt(128))
+    dev = torch.device("cuda")
+    dc = case.to(dev)
+    plan = pka.paged_attn_plan(case.seq_lens, case.block_table, case.query_seq, case.query_pos,
+                               case.page_size, case.num_pages, device=dev)
+    pka.paged_kv_store(plan, dc.new_k, dc.new_v, dc.k_cache, dc.v_cache)
+
+    def fresh():
+        return torch.full((case.num_queries, case.hq, case.dv), float("nan"), dtype=case.dtype, device=dev)
+
+    def call(out):
+        pka.paged_attn_forward(plan, dc.q, dc.k_cache, dc.v_cache, case.scale, out=out)
+
+    warm = fresh()
+    call(warm)                         # kernel attributes are set outside capture
+    torch.cuda.synchronize()
+
+    def serial_then_beside():
+        s = torch.cuda.Stream(dev)
+        with torch.cuda.stream(s):
+            serial = fresh()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):  # no second stream on this thread yet: one after the other
+                call(serial)
+            g.replay()
+            beside = fresh()
+            call(beside)
+        s.synchronize()
+        return serial, beside
+
+    serial, beside = _in_thread(serial_then_beside)
+    assert pka.device_status() == 0
+    assert torch.equal(serial, beside)
+    assert torch.equal(warm, beside)
+    rng = np.random.default_rng(5)
+    npq = len(offs) * chunk
+    qs = np.concatenate([rng.choice(npq, 8, replace=False), npq + rng.choice(len(dctx), 8, replace=False)])
+    rows = np.sort(np.concatenate([q * case.hq + rng.choice(case.hq, 2, replace=False) for q in qs]))
+    ref, _, _, _ = oracle_after_store(case, rows=rows)
+    got = beside.double().cpu().numpy().reshape(-1, case.dv)[rows]
+    assert_close(got, ref, case.dtype, "mixed call, tensor-core decode beside")
