@@ -187,6 +187,26 @@ int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32
 int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t window, int32_t num_sms);
 
 /*
+ * SMs that paged_attn_forward / paged_attn_forward_split leave to the decode
+ * items of this plan while its prefill tiles run on the others (0: the two
+ * kernels run one after the other), on a GPU of num_sms SMs.  Only tiles on
+ * the tensor-core prefill kernel (bf16 or fp16, head_dim = value_dim = 128,
+ * pages of 16, 32, 64 or 128 rows) run beside the decode items.  The pages
+ * describe one call for mixed prefill + decode batches and say nothing of
+ * how its parts share the GPU; this rule is ours.  It models the prefill
+ * kernel at a fixed rate per SM and the decode kernel at a fixed rate per SM
+ * capped while the prefill runs, and keeps the share that shortens the call
+ * by at least 5 %, when both parts would take at least 20 us alone.  The
+ * calls run the decode kernel on a second stream of the calling thread
+ * (created on the first such call that is not being captured), forked from
+ * and joined back into the caller's stream with events.  Pure host function
+ * of the plan; 0 for invalid arguments.
+ */
+int32_t paged_attn_decode_sms_beside_prefill(const pa_plan *plan, int32_t num_heads, int32_t num_kv_heads,
+                                              int32_t head_dim, int32_t value_dim, int32_t causal,
+                                              int32_t window, pa_dtype dtype, int32_t num_sms);
+
+/*
  * One decode step forward, on the device: every query of an uploaded plan
  * moves to position pos + 1 of its sequence, its write slot is taken from the
  * block table and its sequence length grows to cover the new position.  This

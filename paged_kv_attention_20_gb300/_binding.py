@@ -29,7 +29,8 @@ MAX_SPLITS = 64
 
 EXPORTED = ["pa_last_error", "pa_status_string", "pa_abi_version", "paged_attn_plan",
             "pa_plan_device_bytes", "pa_plan_upload", "pa_plan_stage", "pa_plan_destroy", "pa_plan_describe",
-            "pa_workspace_bytes", "paged_attn_split_heuristic", "paged_mla_split_heuristic", "paged_kv_store", "paged_attn_forward",
+            "pa_workspace_bytes", "paged_attn_split_heuristic", "paged_mla_split_heuristic",
+            "paged_attn_decode_sms_beside_prefill", "paged_kv_store", "paged_attn_forward",
             "paged_attn_forward_split", "paged_mla_forward", "pa_plan_advance", "pa_time_next_kernel",
             "pa_device_status"]
 
@@ -79,6 +80,8 @@ def load() -> ctypes.CDLL:
     lib.paged_attn_split_heuristic.restype = i32
     lib.paged_mla_split_heuristic.argtypes = [vp, i32, i32, i32]
     lib.paged_mla_split_heuristic.restype = i32
+    lib.paged_attn_decode_sms_beside_prefill.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, i32]
+    lib.paged_attn_decode_sms_beside_prefill.restype = i32
     lib.paged_kv_store.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int, vp]
     lib.paged_kv_store.restype = ctypes.c_int
     lib.paged_attn_forward.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, i32, i32,
@@ -252,6 +255,17 @@ def paged_mla_split_heuristic(plan: Plan, num_heads: int, num_sms: int | None = 
     if num_sms is None:
         num_sms = torch.cuda.get_device_properties(plan.device or 0).multi_processor_count
     return int(load().paged_mla_split_heuristic(plan.handle, int(num_heads), int(window), int(num_sms)))
+
+
+def paged_attn_decode_sms_beside_prefill(plan: Plan, num_heads: int, num_kv_heads: int, head_dim: int,
+                                         value_dim: int, causal: bool = True, window: int = 0,
+                                         dtype=torch.bfloat16, num_sms: int | None = None) -> int:
+    """SMs an attention call on this plan leaves to its decode items beside the prefill tiles (0: serial)."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(plan.device or 0).multi_processor_count
+    return int(load().paged_attn_decode_sms_beside_prefill(plan.handle, int(num_heads), int(num_kv_heads),
+                                                           int(head_dim), int(value_dim), 1 if causal else 0,
+                                                           int(window), _DTYPES[dtype], int(num_sms)))
 
 
 def paged_kv_store(plan: Plan, new_k, new_v, k_cache, v_cache) -> None:

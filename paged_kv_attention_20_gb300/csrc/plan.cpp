@@ -92,6 +92,9 @@ int device_sms() {
     return sms[dev];
 }
 
+int decode_sms_beside_prefill(const pa_plan *plan, int hq, int hkv, int d, int dv, int causal, int window,
+                              pa_dtype dtype, int sms);
+
 pa::PlanView view_of(const pa_plan *p) {
     pa::PlanView v{};
     v.qmeta = reinterpret_cast<const int4 *>(p->dev + p->off_qmeta);
@@ -398,6 +401,20 @@ int32_t paged_attn_split_heuristic(const pa_plan *plan, int32_t num_heads, int32
     return (int32_t)s;
 }
 
+int32_t paged_attn_decode_sms_beside_prefill(const pa_plan *plan, int32_t num_heads, int32_t num_kv_heads,
+                                              int32_t head_dim, int32_t value_dim, int32_t causal, int32_t window,
+                                              pa_dtype dtype, int32_t num_sms) {
+    if (!plan || num_heads < 1 || num_kv_heads < 1 || head_dim < 1 || value_dim < 1 || !valid_dtype(dtype) ||
+        num_sms < 1)
+        return 0;
+    // only tiles on the tensor-core prefill kernel run beside the decode items
+    const int ps = plan->page_size;
+    if (dtype == PA_F32 || head_dim != 128 || value_dim != 128 || (ps != 16 && ps != 32 && ps != 64 && ps != 128))
+        return 0;
+    return decode_sms_beside_prefill(plan, num_heads, num_kv_heads, head_dim, value_dim, causal, window, dtype,
+                                     num_sms);
+}
+
 int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_t window, int32_t num_sms) {
     if (!plan || num_heads < 1 || num_sms < 1 || plan->queries == 0) return 1;
     // One CTA pair per (query, 128 heads, split), one pair per two SMs; the
@@ -488,7 +505,8 @@ namespace {
 // what is left of the decode then runs on the whole GPU at kHbmBytes.  The
 // share with the shortest modelled call is taken when it saves at least 5 %
 // and both halves are long enough for the fork and join to be noise.
-int decode_sms_beside_prefill(const pa_plan *plan, const pa::AttnArgs &a, int sms) {
+int decode_sms_beside_prefill(const pa_plan *plan, int hq, int hkv, int d, int dv, int causal, int window,
+                              pa_dtype dtype, int sms) {
     constexpr double kPrefillFlopsPerSm = 6.5e12, kDecodeBytesPerSm = 7.2e10, kDecodeBesidePrefill = 2.0e12,
                      kHbmBytes = 6.2e12;
     if (plan->n_decode == 0 || plan->n_tiles == 0 || sms < 8) return 0;
@@ -496,7 +514,7 @@ int decode_sms_beside_prefill(const pa_plan *plan, const pa::AttnArgs &a, int sm
     auto visible = [&](int q) -> double {
         const int seq = w[plan->off_qmeta + 4 * (size_t)q], pos = w[plan->off_qmeta + 4 * (size_t)q + 1];
         int64_t lo, hi;
-        pa::visible_range(pos, w[plan->off_seqlen + seq], a.causal, a.window, lo, hi);
+        pa::visible_range(pos, w[plan->off_seqlen + seq], causal, window, lo, hi);
         return (double)(hi > lo ? hi - lo : 0);
     };
     double keys_p = 0, keys_d = 0;
@@ -505,8 +523,8 @@ int decode_sms_beside_prefill(const pa_plan *plan, const pa::AttnArgs &a, int sm
         for (int i = 0; i < tile[2]; ++i) keys_p += visible(tile[1] + i);
     }
     for (int i = 0; i < plan->n_decode; ++i) keys_d += visible(w[plan->off_decode + i]);
-    const double flops = keys_p * a.hq * 2.0 * (a.d + a.dv);
-    const double bytes = keys_d * a.hkv * (double)(a.d + a.dv) * elem_bytes(a.dtype);
+    const double flops = keys_p * hq * 2.0 * (d + dv);
+    const double bytes = keys_d * hkv * (double)(d + dv) * elem_bytes(dtype);
     const double t_prefill = flops / (kPrefillFlopsPerSm * sms), t_decode = bytes / kHbmBytes;
     if (t_prefill < 20e-6 || t_decode < 20e-6) return 0;
     const double serial = t_prefill + t_decode;
@@ -589,7 +607,8 @@ pa_status attention(const pa_plan *plan, const void *q, const void *k, const voi
         if (tiles) {
             // with splits > 1 both kernels write partials and one merge covers every query
             const int sms = device_sms();
-            const int beside = sms > 0 ? decode_sms_beside_prefill(plan, a, sms) : 0;
+            const int beside =
+                sms > 0 ? decode_sms_beside_prefill(plan, hq, hkv, d, dv, causal, window, dtype, sms) : 0;
             SideStream *side = beside > 0 ? side_stream(st) : nullptr;
             if (side) {
                 // prefill on sms - beside persistent CTAs, launched first so that they

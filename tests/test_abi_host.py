@@ -12,6 +12,7 @@ import os
 import re
 
 import numpy as np
+import torch
 import pytest
 
 import paged_kv_attention_20_gb300 as pka
@@ -266,3 +267,49 @@ def test_status_names_and_per_thread_messages(built_lib):
     t.start()
     t.join()
     assert seen["msg"] == ""                                     # nothing failed on that thread
+
+
+def _mixed_plan(offs, chunk, dctx, ps=16):
+    """Prefill chunks (chunk queries at offsets offs) then one decode query per history in dctx."""
+    lens = [o + chunk for o in offs] + list(dctx)
+    pages = [(n + ps - 1) // ps for n in lens]
+    width = max(pages)
+    table, off = np.full((len(lens), width), -1, dtype=np.int32), 0
+    for i, n in enumerate(pages):
+        table[i, :n] = np.arange(off, off + n)
+        off += n
+    qs, qp = [], []
+    for s, o in enumerate(offs):
+        qs += [s] * chunk
+        qp += list(range(o, o + chunk))
+    for i, n in enumerate(dctx):
+        qs.append(len(offs) + i)
+        qp.append(n - 1)
+    return plan(lens, table, qs, qp, ps, off)
+
+
+def test_decode_sms_beside_prefill(built_lib):
+    """Mixed calls share the SMs only when both halves are large; the share stays a minority."""
+    rng = np.random.default_rng(4)
+    offs = [int(x) for x in rng.integers(0, 4097, size=8)]
+    dctx = [int(x) for x in rng.integers(1024, 4097, size=120)]
+    big = _mixed_plan(offs, 512, dctx)
+    n = pka.paged_attn_decode_sms_beside_prefill(big, 32, 8, 128, 128, num_sms=152)
+    assert 8 <= n <= 60, n                                   # the mixed workload's size: a share for the decode
+    assert pka.paged_attn_decode_sms_beside_prefill(big, 32, 8, 128, 128, dtype=torch.float16, num_sms=152) == n
+    # prefill tiles that the tensor-core prefill kernel does not take (fp32, other head sizes) stay serial
+    assert pka.paged_attn_decode_sms_beside_prefill(big, 32, 8, 128, 128, dtype=torch.float32, num_sms=152) == 0
+    assert pka.paged_attn_decode_sms_beside_prefill(big, 32, 8, 64, 64, num_sms=152) == 0
+    # no decode items, or no prefill tiles, or halves too small: one after the other
+    assert pka.paged_attn_decode_sms_beside_prefill(_mixed_plan(offs, 512, []), 32, 8, 128, 128, num_sms=152) == 0
+    assert pka.paged_attn_decode_sms_beside_prefill(_mixed_plan([], 512, dctx), 32, 8, 128, 128, num_sms=152) == 0
+    small = _mixed_plan([100], 64, [300, 500])
+    assert pka.paged_attn_decode_sms_beside_prefill(small, 32, 8, 128, 128, num_sms=152) == 0
+    # a window shrinks both halves; a tiny window leaves nothing worth splitting
+    assert pka.paged_attn_decode_sms_beside_prefill(big, 32, 8, 128, 128, window=64, num_sms=152) == 0
+    # invalid arguments
+    assert pka.paged_attn_decode_sms_beside_prefill(big, 0, 8, 128, 128, num_sms=152) == 0
+    assert pka.paged_attn_decode_sms_beside_prefill(big, 32, 8, 128, 128, num_sms=0) == 0
+    lib = pka.load()
+    assert lib.paged_attn_decode_sms_beside_prefill(None, 32, 8, 128, 128, 1, 0, 2, 152) == 0
+    assert lib.paged_attn_decode_sms_beside_prefill(big.handle, 32, 8, 128, 128, 1, 0, 7, 152) == 0   # bad dtype
