@@ -118,6 +118,32 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) 
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Transposes the 8 x 8 sixteen-byte chunks held by each group of 8 lanes with
+// three xor butterflies: before, lane j of a group holds chunk c of its own
+// row in ch[4c..4c+3]; after, it holds chunk j of the group's row c there.  A
+// warp storing chunk j of row c from lane j then writes 4 whole 128-byte lines
+// per instruction instead of a 16-byte piece of 32 lines.
+__device__ __forceinline__ void transpose_chunks8(uint32_t (&ch)[32], int lane) {
+    const int jj = lane & 7;
+#pragma unroll
+    for (int b = 1; b < 8; b <<= 1) {
+        const bool hi = (jj & b) != 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            if (c & b) continue;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t send = hi ? ch[4 * c + e] : ch[4 * (c | b) + e];
+                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, b);
+                if (hi)
+                    ch[4 * c + e] = recv;
+                else
+                    ch[4 * (c | b) + e] = recv;
+            }
+        }
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -516,49 +542,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float lsum = l + l_other;
                 const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
                 const int64_t orow = (int64_t)(u.q0 + r) * prm.hq + u.h;
+                const int jj = lane & 7, g = lane & ~7;   // lane in its group of 8, the group's first row
                 if (prm.splits > 1) {
                     const int64_t rows = (int64_t)prm.plan.queries * prm.hq;
-                    float *dst = prm.ws_o + ((int64_t)u.split * rows + orow) * kD + col0;
-#pragma unroll 1
-                    for (int c = 0; c < 64; c += 16) {
-                        uint32_t v[16];
-                        if (u.n_kt > 0) {
-                            tmem_ld16(tmem_o + lane_off + col0 + c, v);
-                            tmem_wait_ld();
-                        }
-                        if (r < u.nq) {
+                    uint32_t vv[64];
+                    if (u.n_kt > 0) {
+                        tmem_ld32(tmem_o + lane_off + col0, vv);
+                        tmem_ld32(tmem_o + lane_off + col0 + 32, vv + 32);
+                        tmem_wait_ld();
+                    } else {
 #pragma unroll
-                            for (int i = 0; i < 16; i += 4)
-                                *reinterpret_cast<float4 *>(dst + c + i) =
-                                    lsum > 0.f ? make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
-                                                             __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv)
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int e = 0; e < 64; ++e) vv[e] = 0u;
+                    }
+                    // fp32 partials: each half of the row's 64 columns is eight 16-byte chunks
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t ch[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            ch[e] = __float_as_uint(lsum > 0.f ? __uint_as_float(vv[32 * hf + e]) * inv : 0.f);
+                        transpose_chunks8(ch, lane);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const int rr = 32 * q4 + g + c;
+                            if (rr < u.nq) {
+                                float *dst = prm.ws_o + ((int64_t)u.split * rows + (int64_t)(u.q0 + rr) * prm.hq + u.h) * kD +
+                                             col0 + 32 * hf + 4 * jj;
+                                *reinterpret_cast<uint4 *>(dst) = make_uint4(ch[4 * c], ch[4 * c + 1], ch[4 * c + 2], ch[4 * c + 3]);
+                            }
                         }
                     }
                     if (r < u.nq && h2 == 0)
                         prm.ws_lse[(int64_t)u.split * rows + orow] =
                             lsum > 0.f ? (m_ref + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
                 } else {
-                T *dst = static_cast<T *>(prm.out) + orow * kD + col0;
                 uint32_t vv[64];
                 tmem_ld32(tmem_o + lane_off + col0, vv);          // all 64 columns, one wait
                 tmem_ld32(tmem_o + lane_off + col0 + 32, vv + 32);
                 tmem_wait_ld();
+                // the row's 64 output columns as eight 16-byte chunks of 16-bit pairs
+                uint32_t ch[32];
 #pragma unroll
-                for (int c = 0; c < 64; c += 16) {
-                    const uint32_t *v = vv + c;
-                    uint4 w0, w1;
-                    w0.x = pack2<T>(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
-                    w0.y = pack2<T>(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
-                    w0.z = pack2<T>(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
-                    w0.w = pack2<T>(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
-                    w1.x = pack2<T>(__uint_as_float(v[8]) * inv, __uint_as_float(v[9]) * inv);
-                    w1.y = pack2<T>(__uint_as_float(v[10]) * inv, __uint_as_float(v[11]) * inv);
-                    w1.z = pack2<T>(__uint_as_float(v[12]) * inv, __uint_as_float(v[13]) * inv);
-                    w1.w = pack2<T>(__uint_as_float(v[14]) * inv, __uint_as_float(v[15]) * inv);
-                    if (r < u.nq) {
-                        reinterpret_cast<uint4 *>(dst + c)[0] = w0;
-                        reinterpret_cast<uint4 *>(dst + c)[1] = w1;
+                for (int e = 0; e < 32; ++e)
+                    ch[e] = pack2<T>(__uint_as_float(vv[2 * e]) * inv, __uint_as_float(vv[2 * e + 1]) * inv);
+                transpose_chunks8(ch, lane);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int rr = 32 * q4 + g + c;                // the row this round stores
+                    if (rr < u.nq) {
+                        T *dst = static_cast<T *>(prm.out) + ((int64_t)(u.q0 + rr) * prm.hq + u.h) * kD + col0 + 8 * jj;
+                        *reinterpret_cast<uint4 *>(dst) = make_uint4(ch[4 * c], ch[4 * c + 1], ch[4 * c + 2], ch[4 * c + 3]);
                     }
                 }
                 }
