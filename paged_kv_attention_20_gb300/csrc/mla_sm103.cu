@@ -425,33 +425,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int64_t rows = (int64_t)prm.plan.queries * prm.heads;
             const int64_t orow = (int64_t)qi * prm.heads + h;
             const float inv = l > 0.f ? 1.f / l : 0.f;
+            // 64 columns per TMEM round trip; the 16-byte chunks are transposed across
+            // each group of 8 lanes so that a warp's store writes whole 128-byte lines
+            const int jj = lane & 7, g = lane & ~7;
 #pragma unroll 1
-            for (int c = 0; c < 256; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem_o + lane_off + c, v);
+            for (int c0 = 0; c0 < 256; c0 += 64) {
+                uint32_t vv[64];
+                tmem_ld32(tmem_o + lane_off + c0, vv);
+                tmem_ld32(tmem_o + lane_off + c0 + 32, vv + 32);
                 tmem_wait_ld();
-                if (!row_ok) continue;
-                const int col = own_col + c;
                 if (prm.splits == 1) {
-                    uint4 w0, w1;
-                    w0.x = pack2<T>(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
-                    w0.y = pack2<T>(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
-                    w0.z = pack2<T>(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
-                    w0.w = pack2<T>(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
-                    w1.x = pack2<T>(__uint_as_float(v[8]) * inv, __uint_as_float(v[9]) * inv);
-                    w1.y = pack2<T>(__uint_as_float(v[10]) * inv, __uint_as_float(v[11]) * inv);
-                    w1.z = pack2<T>(__uint_as_float(v[12]) * inv, __uint_as_float(v[13]) * inv);
-                    w1.w = pack2<T>(__uint_as_float(v[14]) * inv, __uint_as_float(v[15]) * inv);
-                    T *dst = static_cast<T *>(prm.out) + orow * kR + col;
-                    reinterpret_cast<uint4 *>(dst)[0] = w0;
-                    reinterpret_cast<uint4 *>(dst)[1] = w1;
-                } else {
-                    float *dst = prm.ws_o + ((int64_t)split * rows + orow) * kR + col;
+                    uint32_t ch[32];
 #pragma unroll
-                    for (int i = 0; i < 16; i += 4)
-                        *reinterpret_cast<float4 *>(dst + i) =
-                            make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
-                                        __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+                    for (int e = 0; e < 32; ++e)
+                        ch[e] = pack2<T>(__uint_as_float(vv[2 * e]) * inv, __uint_as_float(vv[2 * e + 1]) * inv);
+                    transpose_chunks8(ch, lane);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int hr = hb * kHeads + 32 * warp + g + c;      // the head this round stores
+                        if (hr < prm.heads) {
+                            T *dst = static_cast<T *>(prm.out) + ((int64_t)qi * prm.heads + hr) * kR + own_col + c0 + 8 * jj;
+                            *reinterpret_cast<uint4 *>(dst) = make_uint4(ch[4 * c], ch[4 * c + 1], ch[4 * c + 2], ch[4 * c + 3]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t ch[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ch[e] = __float_as_uint(__uint_as_float(vv[32 * hf + e]) * inv);
+                        transpose_chunks8(ch, lane);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const int hr = hb * kHeads + 32 * warp + g + c;
+                            if (hr < prm.heads) {
+                                float *dst = prm.ws_o + ((int64_t)split * rows + (int64_t)qi * prm.heads + hr) * kR + own_col +
+                                             c0 + 32 * hf + 4 * jj;
+                                *reinterpret_cast<uint4 *>(dst) = make_uint4(ch[4 * c], ch[4 * c + 1], ch[4 * c + 2], ch[4 * c + 3]);
+                            }
+                        }
+                    }
                 }
             }
             if (prm.splits > 1 && rank == 0 && row_ok)

@@ -118,32 +118,6 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) 
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Transposes the 8 x 8 sixteen-byte chunks held by each group of 8 lanes with
-// three xor butterflies: before, lane j of a group holds chunk c of its own
-// row in ch[4c..4c+3]; after, it holds chunk j of the group's row c there.  A
-// warp storing chunk j of row c from lane j then writes 4 whole 128-byte lines
-// per instruction instead of a 16-byte piece of 32 lines.
-__device__ __forceinline__ void transpose_chunks8(uint32_t (&ch)[32], int lane) {
-    const int jj = lane & 7;
-#pragma unroll
-    for (int b = 1; b < 8; b <<= 1) {
-        const bool hi = (jj & b) != 0;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            if (c & b) continue;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t send = hi ? ch[4 * c + e] : ch[4 * (c | b) + e];
-                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, b);
-                if (hi)
-                    ch[4 * c + e] = recv;
-                else
-                    ch[4 * (c | b) + e] = recv;
-            }
-        }
-    }
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
