@@ -306,15 +306,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int h = hb * kHeads + r;
             const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const T *>(prm.q) +
                                                                ((int64_t)qi * prm.heads + h) * kR + own_col);
+            // two rounds of 16 loads in flight (the row is 32 x 16 bytes)
 #pragma unroll 1
-            for (int c = 0; c < 128; c += 16) {
-                uint32_t w[16];
+            for (int c = 0; c < 128; c += 64) {
+                uint32_t w[4][16];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     const uint4 v = h < prm.heads ? src[c / 4 + i] : make_uint4(0, 0, 0, 0);
-                    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+                    w[i / 4][4 * (i % 4)] = v.x; w[i / 4][4 * (i % 4) + 1] = v.y;
+                    w[i / 4][4 * (i % 4) + 2] = v.z; w[i / 4][4 * (i % 4) + 3] = v.w;
                 }
-                tmem_st16(tmem_q + lane_off + c, w);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tmem_st16(tmem_q + lane_off + c + 16 * k, w[k]);
             }
             tmem_wait_st();
             tc_fence_before();
