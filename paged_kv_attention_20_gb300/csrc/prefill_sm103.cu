@@ -15,7 +15,9 @@
 //   warps 0-7  softmax / O correction / epilogue: query row r (TMEM lane r) is
 //              shared by warps r/32 and r/32+4, each taking 64 of the 128 key
 //              (and output) columns; row maxima and sums cross over shared memory;
-//   warps 8/10 TMA producers: Q of each unit and K tiles (warp 8), V tiles (warp 10)
+//   warps 8/10 TMA producers: Q of each unit and K tiles (warp 8, which also works
+//              out each unit's parameters and leaves them in shared memory for
+//              the other roles), V tiles (warp 10)
 //              of 128 keys gathered page by page through the block table
 //              (one box per page and 64-column half, 128-byte swizzle), each
 //              through its own ring, so K is released once S is computed; the
@@ -81,6 +83,9 @@ struct Smem {
     float xred[2][2 * kM];         // row-max / row-sum exchange between the two warps of a row,
                                    // slot n % 2 for exchange n
     uint64_t xa[2][4];             // per slot and lane quarter: both warps' values written
+    int32_t up[4][12];             // parameters of unit i in slot i % 4, written by the K producer
+    uint64_t up_full[4];           // slot written
+    uint64_t up_empty[4];          // slot read by every other role (11 arrivals)
     uint32_t tmem_base;
 };
 
@@ -211,6 +216,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         return ui < units ? ui : units;
     };
 
+    // Unit parameters come from dependent loads of plan metadata (~700 cycles).
+    // The K producer, which runs furthest ahead, computes them and leaves them
+    // in shared memory; every other role reads them from there.
+    auto publish_unit = [&](int i, const Unit &u) -> bool {
+        const int sl = i & 3;
+        if (i >= 4 && !mbar_wait(&s.up_empty[sl], ((i >> 2) - 1) & 1)) return false;
+        int32_t *p = s.up[sl];
+        p[0] = u.split; p[1] = u.h; p[2] = u.kvh; p[3] = u.q0; p[4] = u.nq;
+        p[5] = u.pos0; p[6] = u.seq_len; p[7] = u.kt0; p[8] = u.n_kt;
+        const uint64_t t = reinterpret_cast<uint64_t>(u.trow);
+        p[9] = (int32_t)(uint32_t)t;
+        p[10] = (int32_t)(uint32_t)(t >> 32);
+        mbar_arrive(&s.up_full[sl]);
+        return true;
+    };
+    // every lane of the calling warp (or the one calling lane) waits and reads;
+    // `one` arrives for the warp once all its lanes have read
+    auto read_unit = [&](int i, Unit &u, bool whole_warp) -> bool {
+        const int sl = i & 3;
+        bool ok = mbar_wait(&s.up_full[sl], (i >> 2) & 1);
+        if (whole_warp) ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        const int32_t *p = s.up[sl];
+        u.split = p[0]; u.h = p[1]; u.kvh = p[2]; u.q0 = p[3]; u.nq = p[4];
+        u.pos0 = p[5]; u.seq_len = p[6]; u.kt0 = p[7]; u.n_kt = p[8];
+        u.trow = reinterpret_cast<const int32_t *>((uint64_t)(uint32_t)p[9] | ((uint64_t)(uint32_t)p[10] << 32));
+        if (whole_warp) __syncwarp();
+        if (!whole_warp || lane == 0) mbar_arrive(&s.up_empty[sl]);
+        return true;
+    };
+
     if (tid == 0) {
         mbar_init(&s.q_full, 1);
         mbar_init(&s.q_empty, 1);
@@ -228,6 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&s.xa[1][i], 64);
         }
         for (int i = 0; i < 3; ++i) mbar_init(&s.o_done[i], 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&s.up_full[i], 1);
+            mbar_init(&s.up_empty[i], 11);      // V producer, two MMA issuers, eight softmax warps
+        }
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -262,7 +302,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         int gt = 0;                                        // tiles streamed so far (all units)
         bool go = true;
         for (int i = 0; go && unit_of(i) < units; ++i) {
-            const Unit u = unit_at(unit_of(i));
+            Unit u;
+            if (is_k) {
+                u = unit_at(unit_of(i));
+                if (lane == 0 && !publish_unit(i, u)) {
+                    set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
+                    go = false;
+                }
+                go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+                if (!go) break;
+            } else if (!read_unit(i, u, true)) {
+                set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
+                break;
+            }
             if (is_k && lane == 0) {
                 if (i > 0 && !mbar_wait(&s.q_empty, (i - 1) & 1)) {
                     set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_TMA);
@@ -331,7 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t idesc_s = idesc_f16(kM, kN, prm.bf16 != 0, false, false);
                 const uint64_t q_desc = smem_desc(smem_u32(s.q), 16, 1024, kLayoutSwizzle128B);
                 for (int i = 0; ok && unit_of(i) < units; ++i) {
-                    const Unit u = unit_at(unit_of(i));
+                    Unit u;
+                    if (!read_unit(i, u, false)) { ok = false; break; }
                     if (!mbar_wait(&s.q_full, i & 1)) { ok = false; break; }
                     for (int kt = 0; kt < u.n_kt; ++kt, ++gt) {
                         const int st = gt % kStages, sb = gt % 3;
@@ -358,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 const uint32_t idesc_o = idesc_f16(kM, kD, prm.bf16 != 0, false, true);
                 for (int i = 0; ok && unit_of(i) < units; ++i) {
-                    const Unit u = unit_at(unit_of(i));
+                    Unit u;
+                    if (!read_unit(i, u, false)) { ok = false; break; }
                     if (i > 0 && !mbar_wait(&s.o_free, (i - 1) & 1)) { ok = false; break; }
                     for (int kt = 0; kt < u.n_kt; ++kt, ++gt) {
                         const int st = gt % kStages;
@@ -402,10 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++xphase;
             return true;
         };
-        // a unit's parameters come from dependent loads of plan metadata; the
-        // next unit's are fetched before this unit's epilogue, so their latency
-        // overlaps it instead of delaying the next unit's first softmax
-        Unit u = unit_of(0) < units ? unit_at(unit_of(0)) : Unit{};
+        // a unit's parameters come from the K producer through shared memory; the
+        // next unit's are read before this unit's epilogue
+        Unit u{};
+        if (unit_of(0) < units) ok = read_unit(0, u, true);
+        if (!ok) set_timeout(s, prm.status, PA_DEVICE_TIMEOUT_SOFTMAX);
         for (int i = 0; ok && unit_of(i) < units; ++i) {
             int64_t row_j0 = 0, row_j1 = 0;           // this row's keys in this split: [vis_lo, vis_end)
             if (r < u.nq) row_keys(u, u.pos0 + r, row_j0, row_j1);   // rows past the tile's queries see nothing
@@ -501,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&s.p_ready[gt % 3]);
             }
             const bool more = unit_of(i + 1) < units;
-            const Unit nu = more ? unit_at(unit_of(i + 1)) : u;
+            Unit nu = u;
+            if (more && ok) ok = read_unit(i + 1, nu, true);
             if (ok && u.n_kt > 0)
                 ok = __all_sync(0xffffffffu, mbar_wait(&s.o_done[(gt - 1) % 3], ((gt - 1) / 3) & 1));
             float l_other = 0.f;
