@@ -175,3 +175,55 @@ def test_mixed_call_tensor_core_decode_beside(cuda_device):
     ref, _, _, _ = oracle_after_store(case, rows=rows)
     got = beside.double().cpu().numpy().reshape(-1, case.dv)[rows]
     assert_close(got, ref, case.dtype, "mixed call, tensor-core decode beside")
+
+
+@pytest.mark.parametrize("dtype,causal", [(torch.float16, True), (torch.bfloat16, False)])
+def test_mixed_call_beside_fp16_and_non_causal(cuda_device, dtype, causal):
+    # the mixed workload's layout in fp16, and non-causal (every query sees its whole sequence)
+    base = mixed_prefill_decode_bf16()
+    offs, chunk = base.meta["prefill_offsets"], base.meta["chunk"]
+    npf = len(offs)
+    dctx = [int(n) for n in base.seq_lens[npf:]]
+    seq_lens = [o + chunk for o in offs] + dctx
+    queries = [(s, o + i) for s, o in enumerate(offs) for i in range(chunk)]
+    queries += [(npf + s, n - 1) for s, n in enumerate(dctx)]
+    case = build_case("mixed_variant", 43, seq_lens, queries, 32, 8, 128, 128, 16, dtype, 1 / math.sqrt(128),
+                      causal=causal)
+    dev = torch.device("cuda")
+    dc = case.to(dev)
+    plan = pka.paged_attn_plan(case.seq_lens, case.block_table, case.query_seq, case.query_pos,
+                               case.page_size, case.num_pages, device=dev)
+    pka.paged_kv_store(plan, dc.new_k, dc.new_v, dc.k_cache, dc.v_cache)
+    assert pka.paged_attn_decode_sms_beside_prefill(plan, 32, 8, 128, 128, causal=causal, dtype=dtype) > 0
+
+    def fresh():
+        return torch.full((case.num_queries, case.hq, case.dv), float("nan"), dtype=case.dtype, device=dev)
+
+    def call(out):
+        pka.paged_attn_forward(plan, dc.q, dc.k_cache, dc.v_cache, case.scale, causal=causal, out=out)
+
+    beside = fresh()
+    call(beside)                       # kernel attributes are set outside capture
+
+    def serial_form():
+        s = torch.cuda.Stream(dev)
+        with torch.cuda.stream(s):
+            out = fresh()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):  # no second stream on this thread yet: one after the other
+                call(out)
+            g.replay()
+        s.synchronize()
+        return out
+
+    serial = _in_thread(serial_form)
+    torch.cuda.synchronize()
+    assert pka.device_status() == 0
+    assert torch.equal(serial, beside)
+    rng = np.random.default_rng(11)
+    npq = npf * chunk
+    qs = np.concatenate([rng.choice(npq, 8, replace=False), npq + rng.choice(len(dctx), 8, replace=False)])
+    rows = np.sort(np.concatenate([q * case.hq + rng.choice(case.hq, 2, replace=False) for q in qs]))
+    ref, _, _, _ = oracle_after_store(case, rows=rows, causal=causal)
+    got = beside.double().cpu().numpy().reshape(-1, case.dv)[rows]
+    assert_close(got, ref, case.dtype, f"mixed call beside ({dtype}, causal={causal})")
