@@ -25,6 +25,9 @@ struct pa_plan {
     std::vector<int32_t> words;       // host copy of the device metadata
     size_t off_qmeta = 0, off_seqlen = 0, off_table = 0, off_decode = 0, off_tiles = 0, off_order = 0;
     const int32_t *dev = nullptr;     // caller's device copy (after upload)
+    // visible keys of the prefill tiles' queries and of the decode items, without
+    // a window, non-causal [0] and causal [1] (the mixed call's SM share needs them)
+    double keys_tiles[2] = {0, 0}, keys_decode[2] = {0, 0};
 };
 
 namespace {
@@ -102,6 +105,23 @@ int device_sms() {
 
 int decode_sms_beside_prefill(const pa_plan *plan, int hq, int hkv, int d, int dv, int causal, int window,
                               pa_dtype dtype, int sms);
+
+// Visible keys summed over the prefill tiles' queries and over the decode items.
+void visible_key_sums(const pa_plan *plan, int causal, int window, double &keys_tiles, double &keys_decode) {
+    const int32_t *w = plan->words.data();
+    auto visible = [&](int q) -> double {
+        const int seq = w[plan->off_qmeta + 4 * (size_t)q], pos = w[plan->off_qmeta + 4 * (size_t)q + 1];
+        int64_t lo, hi;
+        pa::visible_range(pos, w[plan->off_seqlen + seq], causal, window, lo, hi);
+        return (double)(hi > lo ? hi - lo : 0);
+    };
+    keys_tiles = keys_decode = 0;
+    for (int t = 0; t < plan->n_tiles; ++t) {
+        const int32_t *tile = w + plan->off_tiles + 4 * (size_t)t;
+        for (int i = 0; i < tile[2]; ++i) keys_tiles += visible(tile[1] + i);
+    }
+    for (int i = 0; i < plan->n_decode; ++i) keys_decode += visible(w[plan->off_decode + i]);
+}
 
 pa::PlanView view_of(const pa_plan *p) {
     pa::PlanView v{};
@@ -323,6 +343,7 @@ pa_status paged_attn_plan(const int32_t *seq_lens, int32_t num_seqs, const int32
                          [&](int32_t a, int32_t b) { return query_pos[a] > query_pos[b]; });
         if (num_queries) std::memcpy(w + p->off_order, order.data(), sizeof(int32_t) * order.size());
     }
+    for (int c = 0; c < 2; ++c) visible_key_sums(p, c, 0, p->keys_tiles[c], p->keys_decode[c]);
     *out_plan = p;
     return PA_OK;
 }
@@ -518,19 +539,13 @@ int decode_sms_beside_prefill(const pa_plan *plan, int hq, int hkv, int d, int d
     constexpr double kPrefillFlopsPerSm = 6.5e12, kDecodeBytesPerSm = 7.2e10, kDecodeBesidePrefill = 2.0e12,
                      kHbmBytes = 6.2e12;
     if (plan->n_decode == 0 || plan->n_tiles == 0 || sms < 8) return 0;
-    const int32_t *w = plan->words.data();
-    auto visible = [&](int q) -> double {
-        const int seq = w[plan->off_qmeta + 4 * (size_t)q], pos = w[plan->off_qmeta + 4 * (size_t)q + 1];
-        int64_t lo, hi;
-        pa::visible_range(pos, w[plan->off_seqlen + seq], causal, window, lo, hi);
-        return (double)(hi > lo ? hi - lo : 0);
-    };
-    double keys_p = 0, keys_d = 0;
-    for (int t = 0; t < plan->n_tiles; ++t) {
-        const int32_t *tile = w + plan->off_tiles + 4 * (size_t)t;
-        for (int i = 0; i < tile[2]; ++i) keys_p += visible(tile[1] + i);
+    double keys_p, keys_d;
+    if (window == 0) {          // worked out when the plan was built
+        keys_p = plan->keys_tiles[causal ? 1 : 0];
+        keys_d = plan->keys_decode[causal ? 1 : 0];
+    } else {
+        visible_key_sums(plan, causal, window, keys_p, keys_d);
     }
-    for (int i = 0; i < plan->n_decode; ++i) keys_d += visible(w[plan->off_decode + i]);
     const double flops = keys_p * hq * 2.0 * (d + dv);
     const double bytes = keys_d * hkv * (double)(d + dv) * elem_bytes(dtype);
     const double t_prefill = flops / (kPrefillFlopsPerSm * sms), t_decode = bytes / kHbmBytes;
