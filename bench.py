@@ -293,9 +293,10 @@ def _pipelined_e2e(step, names, host_src, device, steps: int, warmup: int, pre=N
     """Replays a step through the public API from host buffers, software-
     pipelined as a serving loop runs it.  Two CUDA graphs alternate.  Graph p
     runs `pre` (if any), paged_kv_store and the attention on device input set
-    p into device output p; beside it, on a second stream, it copies the next
-    step's inputs from pinned host set 1-p into device set 1-p and the
-    previous step's output from device output 1-p into pinned host buffer 1-p.
+    p into device output p; beside it, on two more streams (one per copy
+    direction), it copies the next step's inputs from pinned host set 1-p into
+    device set 1-p and the previous step's output from device output 1-p into
+    pinned host buffer 1-p.
     The host enqueues step i+1, then waits for step i.  Every step thus moves
     one step's inputs host-to-device and one output device-to-host, and both
     copies overlap a step's kernels; the timed region ends with the copy of
@@ -310,21 +311,24 @@ def _pipelined_e2e(step, names, host_src, device, steps: int, warmup: int, pre=N
     hsets = [{k: host_src[k].pin_memory() for k in names} for _ in range(2)]
     outs = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
     stream = torch.cuda.current_stream(device)
-    copier = torch.cuda.Stream(device)
+    h2d, d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)   # one per copy direction
 
     def body(p):
         cur = torch.cuda.current_stream(device)
-        copier.wait_stream(cur)
-        with torch.cuda.stream(copier):
+        h2d.wait_stream(cur)
+        d2h.wait_stream(cur)
+        with torch.cuda.stream(h2d):
             for k in names:
                 getattr(dsets[1 - p], k).copy_(hsets[1 - p][k], non_blocking=True)
+        with torch.cuda.stream(d2h):
             outs[1 - p].copy_(douts[1 - p], non_blocking=True)
         step.dc, step.out = dsets[p], douts[p]
         if pre:
             pre()
         step.store()
         step.attend()
-        cur.wait_stream(copier)
+        cur.wait_stream(h2d)
+        cur.wait_stream(d2h)
 
     side = torch.cuda.Stream(device)
     side.wait_stream(stream)
@@ -366,8 +370,8 @@ def _pipelined_e2e(step, names, host_src, device, steps: int, warmup: int, pre=N
     return dt, outs[last].clone()
 
 
-PIPELINE_MODE = ("two CUDA graphs alternate; graph p runs the step on device set p while a second stream "
-                 "copies the next step's inputs from pinned host set 1-p and the previous step's output "
+PIPELINE_MODE = ("two CUDA graphs alternate; graph p runs the step on device set p while two more streams "
+                 "copy the next step's inputs from pinned host set 1-p and the previous step's output "
                  "into pinned host buffer 1-p; the host enqueues step i+1 before waiting for step i; the "
                  "timed region ends with the copy of the last output")
 
