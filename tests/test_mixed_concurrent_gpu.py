@@ -177,9 +177,11 @@ def test_mixed_call_tensor_core_decode_beside(cuda_device):
     assert_close(got, ref, case.dtype, "mixed call, tensor-core decode beside")
 
 
-@pytest.mark.parametrize("dtype,causal", [(torch.float16, True), (torch.bfloat16, False)])
-def test_mixed_call_beside_fp16_and_non_causal(cuda_device, dtype, causal):
-    # the mixed workload's layout in fp16, and non-causal (every query sees its whole sequence)
+@pytest.mark.parametrize("dtype,causal,window", [(torch.float16, True, 0), (torch.bfloat16, False, 0),
+                                                 (torch.bfloat16, True, 2048)])
+def test_mixed_call_beside_fp16_and_non_causal(cuda_device, dtype, causal, window):
+    # the mixed workload's layout in fp16, non-causal (every query sees its whole sequence),
+    # and under a sliding window
     base = mixed_prefill_decode_bf16()
     offs, chunk = base.meta["prefill_offsets"], base.meta["chunk"]
     npf = len(offs)
@@ -194,13 +196,15 @@ def test_mixed_call_beside_fp16_and_non_causal(cuda_device, dtype, causal):
     plan = pka.paged_attn_plan(case.seq_lens, case.block_table, case.query_seq, case.query_pos,
                                case.page_size, case.num_pages, device=dev)
     pka.paged_kv_store(plan, dc.new_k, dc.new_v, dc.k_cache, dc.v_cache)
-    assert pka.paged_attn_decode_sms_beside_prefill(plan, 32, 8, 128, 128, causal=causal, dtype=dtype) > 0
+    assert pka.paged_attn_decode_sms_beside_prefill(plan, 32, 8, 128, 128, causal=causal, window=window,
+                                                    dtype=dtype) > 0
 
     def fresh():
         return torch.full((case.num_queries, case.hq, case.dv), float("nan"), dtype=case.dtype, device=dev)
 
     def call(out):
-        pka.paged_attn_forward(plan, dc.q, dc.k_cache, dc.v_cache, case.scale, causal=causal, out=out)
+        pka.paged_attn_forward(plan, dc.q, dc.k_cache, dc.v_cache, case.scale, causal=causal, window=window,
+                               out=out)
 
     beside = fresh()
     call(beside)                       # kernel attributes are set outside capture
@@ -224,6 +228,6 @@ def test_mixed_call_beside_fp16_and_non_causal(cuda_device, dtype, causal):
     npq = npf * chunk
     qs = np.concatenate([rng.choice(npq, 8, replace=False), npq + rng.choice(len(dctx), 8, replace=False)])
     rows = np.sort(np.concatenate([q * case.hq + rng.choice(case.hq, 2, replace=False) for q in qs]))
-    ref, _, _, _ = oracle_after_store(case, rows=rows, causal=causal)
+    ref, _, _, _ = oracle_after_store(case, rows=rows, causal=causal, window=window)
     got = beside.double().cpu().numpy().reshape(-1, case.dv)[rows]
-    assert_close(got, ref, case.dtype, f"mixed call beside ({dtype}, causal={causal})")
+    assert_close(got, ref, case.dtype, f"mixed call beside ({dtype}, causal={causal}, window={window})")
