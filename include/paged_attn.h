@@ -198,8 +198,10 @@ int32_t paged_mla_split_heuristic(const pa_plan *plan, int32_t num_heads, int32_
  * capped while the prefill runs, and keeps the share that shortens the call
  * by at least 5 %, when both parts would take at least 20 us alone.  The
  * calls run the decode kernel on a second stream of the calling thread
- * (created on the first such call that is not being captured), forked from
- * and joined back into the caller's stream with events.  Pure host function
+ * (created on the first such call that is not being captured and kept for
+ * the thread's life, like the status word: a process that resets the device
+ * must not call the library on it again), forked from and joined back into
+ * the caller's stream with events.  Pure host function
  * of the plan; 0 for invalid arguments.
  */
 int32_t paged_attn_decode_sms_beside_prefill(const pa_plan *plan, int32_t num_heads, int32_t num_kv_heads,
