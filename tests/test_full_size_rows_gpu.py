@@ -64,3 +64,29 @@ def test_mla_longest_and_shortest_histories_all_heads(cuda_device):
     got = _run(case, splits)[rows]
     ref, _, _, _ = oracle_after_store(case, rows=rows)
     assert_close(got, ref, case.dtype, f"mla: 16 queries x 128 heads, splits {splits}")
+
+
+@pytest.mark.parametrize("splits", [2, 3])
+def test_mla_split_partials_full_size(cuda_device, splits):
+    """The MLA workload with its histories split: the fp32 partials (written through the
+    epilogue's lane-group transpose) and the merge, on the longest histories' heads."""
+    case = mla_decode_bf16()
+    order = np.argsort(case.query_pos)
+    queries = np.concatenate([order[-4:], order[:2]])
+    rows = (queries[:, None] * case.hq + np.arange(case.hq)[None, :]).reshape(-1)
+    got = _run(case, splits)[rows]
+    ref, _, _, _ = oracle_after_store(case, rows=rows)
+    assert_close(got, ref, case.dtype, f"mla: 6 queries x 128 heads, splits {splits}")
+
+
+def test_mixed_split_partials_longest_chunk(cuda_device):
+    """The mixed workload at 3 splits: the prefill kernel's fp32 partials for every row of
+    the longest chunk, merged with the decode items' partials."""
+    case = mixed_prefill_decode_bf16()
+    chunk, offs = case.meta["chunk"], case.meta["prefill_offsets"]
+    longest = int(np.argmax(offs))
+    first = longest * chunk
+    rows = (np.arange(first, first + chunk)[:, None] * case.hq + np.arange(case.hq)[None, :]).reshape(-1)
+    got = _run(case, 3)[rows]
+    ref, _, _, _ = oracle_after_store(case, rows=rows)
+    assert_close(got, ref, case.dtype, "mixed: longest chunk, splits 3")
